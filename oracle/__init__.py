@@ -1,0 +1,6 @@
+"""CPU fp64 oracle for the exact softmax attention forward.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
+benchmark's CPU-baseline and reference legs, never by the product path.
+"""
+from .oracle import Oracle, build, compile_source, default_threads, forward, probs  # noqa: F401

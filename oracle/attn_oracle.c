@@ -1,0 +1,238 @@
+/*
+ * Exact softmax attention, plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file; only the test suite, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header or constant with the CUDA path.
+ *
+ * What it computes (the plain definition, no tiling, no online recurrence):
+ *   for every query row i of every (b, h):
+ *     s_j   = scale * sum_t q[i,t] * k[j,t]            for all keys j < N
+ *             ("understand-flashattention", forward-pass formulas S = Q K^T;
+ *              the scale is applied to the scores after the matmul and before
+ *              the mask, as in "PyTorch profiling part 3: attention",
+ *              section "Naive attention", steps 1-3)
+ *     vis_j = (!causal || j <= i) && j < key_len[b]    (same section, step 3:
+ *              masked scores are -inf; the key-padding form follows the
+ *              "Linear Attention CUDA kernel" page, key_lengths mask on K)
+ *     m     = max over visible j of s_j                 ("understand-flashattention",
+ *     l     = sum over visible j of exp(s_j - m)         section "numerically stable
+ *     p_j   = exp(s_j - m) / l  (0 for masked j)         softmax", key statistics)
+ *     o     = sum_j p_j v[j,:]                          (forward pass, O = P V)
+ *     lse   = m + log(l)   (natural log)                ("understand-flashattention",
+ *                                                        logsumexp derivation, step 8)
+ *   A row with no visible key gets o = 0 and lse = -inf: the "safe softmax"
+ *   convention of "PyTorch profiling part 3: attention", section "The safe softmax".
+ *
+ * Masked terms are left out of the max and the sum rather than carried as
+ * -inf; the two readings give the same numbers and this one needs no inf
+ * arithmetic.
+ *
+ * Inputs are bfloat16 bit patterns; each is widened to double exactly
+ * (a bf16 value is the upper half of an IEEE binary32).
+ *
+ * Threads: plain pthreads over independent query rows.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    int64_t B, H, N, d;
+    double scale;
+    int causal;
+    const int32_t *key_len;
+    const int64_t *rows;   /* flat row ids into [B*H*N], or NULL for all */
+    int64_t n_rows;
+    double *o, *lse;
+    int64_t begin, end;    /* this worker's slice of [0, n_rows) */
+    int status;
+} oracle_job;
+
+/* One query row, the plain definition written out. */
+static void one_row(const oracle_job *J, int64_t flat, double *s, double *qrow,
+                    double *o_out, double *lse_out)
+{
+    const int64_t N = J->N, d = J->d;
+    const int64_t bh = flat / N;
+    const int64_t i = flat % N;
+    const int64_t b = bh / J->H;
+    const uint16_t *qp = J->q + flat * d;
+    const uint16_t *kp = J->k + bh * N * d;
+    const uint16_t *vp = J->v + bh * N * d;
+
+    int64_t klen = N;
+    if (J->key_len) {
+        klen = J->key_len[b];
+        if (klen < 0) klen = 0;
+        if (klen > N) klen = N;
+    }
+
+    for (int64_t t = 0; t < d; ++t) qrow[t] = bf16_bits_to_double(qp[t]);
+
+    /* 1. the full score row, scaled */
+    for (int64_t j = 0; j < N; ++j) {
+        double acc = 0.0;
+        const uint16_t *kj = kp + j * d;
+        for (int64_t t = 0; t < d; ++t) acc += qrow[t] * bf16_bits_to_double(kj[t]);
+        s[j] = J->scale * acc;
+    }
+
+    /* 2.-3. visibility, row max, normaliser */
+    int any = 0;
+    double m = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        int vis = (!J->causal || j <= i) && j < klen;
+        if (!vis) continue;
+        if (!any || s[j] > m) m = s[j];
+        any = 1;
+    }
+    for (int64_t t = 0; t < d; ++t) o_out[t] = 0.0;
+    if (!any) {
+        *lse_out = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        int vis = (!J->causal || j <= i) && j < klen;
+        if (vis) l += exp(s[j] - m);
+    }
+
+    /* 4. o = sum_j p_j v_j */
+    for (int64_t j = 0; j < N; ++j) {
+        int vis = (!J->causal || j <= i) && j < klen;
+        if (!vis) continue;
+        double p = exp(s[j] - m) / l;
+        const uint16_t *vj = vp + j * d;
+        for (int64_t t = 0; t < d; ++t) o_out[t] += p * bf16_bits_to_double(vj[t]);
+    }
+
+    /* 5. natural-log LSE */
+    *lse_out = m + log(l);
+}
+
+static void *worker(void *arg)
+{
+    oracle_job *J = (oracle_job *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)J->N);
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)J->d);
+    if (!s || !qrow) {
+        free(s);
+        free(qrow);
+        J->status = 2;
+        return NULL;
+    }
+    for (int64_t r = J->begin; r < J->end; ++r) {
+        int64_t flat = J->rows ? J->rows[r] : r;
+        one_row(J, flat, s, qrow, J->o + r * J->d, J->lse + r);
+    }
+    free(s);
+    free(qrow);
+    J->status = 0;
+    return NULL;
+}
+
+/*
+ * q, k, v : bf16 bits, [B, H, N, d] contiguous.
+ * key_len : int32 [B] or NULL (all N keys).
+ * rows    : flat row ids (b*H + h)*N + i to evaluate, or NULL for every row.
+ * o       : double [n_rows, d] (n_rows = B*H*N when rows is NULL).
+ * lse     : double [n_rows].
+ * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ */
+int fattn_oracle_forward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         int64_t B, int64_t H, int64_t N, int64_t d, double scale,
+                         int causal, const int32_t *key_len, const int64_t *rows,
+                         int64_t n_rows, double *o, double *lse, int n_threads)
+{
+    if (!q || !k || !v || !o || !lse || B < 0 || H < 0 || N < 0 || d <= 0) return 1;
+    const int64_t total = B * H * N;
+    if (!rows) n_rows = total;
+    if (n_rows < 0) return 1;
+    if (rows)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= total) return 1;
+    if (n_rows == 0) return 0;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+    if ((int64_t)n_threads > n_rows) n_threads = (int)n_rows;
+
+    oracle_job jobs[256];
+    pthread_t tids[256];
+    int started[256];
+    for (int w = 0; w < n_threads; ++w) {
+        oracle_job *J = &jobs[w];
+        J->q = q; J->k = k; J->v = v;
+        J->B = B; J->H = H; J->N = N; J->d = d;
+        J->scale = scale; J->causal = causal; J->key_len = key_len;
+        J->rows = rows; J->n_rows = n_rows; J->o = o; J->lse = lse;
+        /* contiguous blocks: every row costs the same (a full score row) */
+        J->begin = n_rows * w / n_threads;
+        J->end = n_rows * (w + 1) / n_threads;
+        J->status = 0;
+    }
+    int rc = 0;
+    for (int w = 0; w < n_threads; ++w) {
+        started[w] = (n_threads > 1) && pthread_create(&tids[w], NULL, worker, &jobs[w]) == 0;
+        if (!started[w]) worker(&jobs[w]);
+    }
+    for (int w = 0; w < n_threads; ++w) {
+        if (started[w]) pthread_join(tids[w], NULL);
+        if (jobs[w].status) rc = jobs[w].status;
+    }
+    return rc;
+}
+
+/*
+ * The full probability matrix P (and the scaled score matrix S) of one
+ * (b, h), for small N: p[i*N + j] = softmax row i, 0 where masked; a row with
+ * no visible key is all zero.  s may be NULL.  Same definition as above.
+ */
+int fattn_oracle_probs(const uint16_t *q, const uint16_t *k, int64_t B, int64_t H,
+                       int64_t N, int64_t d, double scale, int causal,
+                       const int32_t *key_len, int64_t b, int64_t h, double *p, double *s)
+{
+    if (!q || !k || !p || b < 0 || b >= B || h < 0 || h >= H || N < 0 || d <= 0) return 1;
+    int64_t klen = N;
+    if (key_len) {
+        klen = key_len[b];
+        if (klen < 0) klen = 0;
+        if (klen > N) klen = N;
+    }
+    const uint16_t *qp = q + (b * H + h) * N * d;
+    const uint16_t *kp = k + (b * H + h) * N * d;
+    for (int64_t i = 0; i < N; ++i) {
+        double *prow = p + i * N;
+        int any = 0;
+        double m = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < d; ++t)
+                acc += bf16_bits_to_double(qp[i * d + t]) * bf16_bits_to_double(kp[j * d + t]);
+            prow[j] = scale * acc;
+            if (s) s[i * N + j] = prow[j];
+            int vis = (!causal || j <= i) && j < klen;
+            if (vis && (!any || prow[j] > m)) m = prow[j];
+            if (vis) any = 1;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            int vis = (!causal || j <= i) && j < klen;
+            prow[j] = (vis && any) ? exp(prow[j] - m) : 0.0;
+            l += prow[j];
+        }
+        for (int64_t j = 0; j < N; ++j) prow[j] = any ? prow[j] / l : 0.0;
+    }
+    return 0;
+}
