@@ -1,0 +1,367 @@
+"""Attention-forward benchmark: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one exact attention forward (the whole fused kernel: tile loads,
+scores, masks, online softmax, correction, PV, epilogue) over the workload's
+synthetic inputs, already resident in HBM.  Between timed steps the L2 cache
+is flushed by writing a 256 MiB buffer; each step's kernel is timed with CUDA
+events on the stream it is launched on, and the steps' times are summed.
+
+Default workload: B=2, H=16, N=4096, d=128, causal, bf16, seed 2.  Metric:
+attention forward TFLOP/s with causal FLOPs counted at half (4*B*H*N^2*d/2).
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
+workload (independent heads/batches need no exchange; no collective touches
+the data path), timed between barriers; `value` is the FLOPs of all ranks
+divided by the slowest rank's time (weak scaling).
+
+--impl reference times the fp64 CPU oracle (plain loops, the definition of the
+result) on the host cores, on a bounded sample of query rows of the same
+workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_softmax_attention_fattn_gb300.inputs import HEADLINE, WORKLOADS, causal_flops, make_inputs  # noqa: E402
+
+KERNEL_NAME = "fattn_fwd_kernel"
+METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 bf16 dense peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_BF16_TFLOPS = 1900.0
+CSRC = os.path.join(ROOT, "exact_softmax_attention_fattn_gb300", "csrc")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str, float | None]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured", float(pk.get("hbm_gbs")) if pk.get("hbm_gbs") else None
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback", 6800.0
+
+
+def ncu_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.txt")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": float(max(power)) if power else None}
+
+
+# ---------------------------------------------------------------- oracle leg
+def oracle_sample(workload: str, seconds: float, x=None):
+    """Time the fp64 oracle on a bounded sample of query rows; returns
+    (TFLOP/s, rows, seconds, threads, description)."""
+    import oracle
+
+    w = WORKLOADS[workload]
+    if x is None:
+        x = make_inputs(w)
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(1234)
+    total_rows = w.B * w.H * w.N
+
+    def visible(rows):
+        i = rows % w.N
+        b = rows // (w.H * w.N)
+        kl = np.full(rows.shape, w.N) if x.key_len is None else np.clip(x.key_len[b], 0, w.N)
+        return np.minimum(kl, i + 1) if w.causal else kl
+
+    def run(n):
+        rows = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.forward(x.q, x.k, x.v, w.softmax_scale, w.causal, key_len=x.key_len, rows=rows, threads=threads)
+        return rows, time.perf_counter() - t0
+
+    rows, dt = run(threads * 2)
+    n = int(max(threads, min(total_rows, len(rows) * seconds / max(dt, 1e-6))))
+    rows, dt = run(n)
+    flops = 4.0 * w.d * float(np.sum(visible(rows)))
+    desc = (f"{len(rows)} random query rows of {total_rows} ({workload}), full fp64 score rows, "
+            f"{threads} threads")
+    return flops / dt / 1e12, len(rows), dt, threads, desc
+
+
+def reference_arm(args, rank: int, world: int):
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w)
+    per_step = max(1.0, min(20.0, 100.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, per_step / 4, x)
+    vals, secs, rows_tot = [], 0.0, 0
+    threads, desc = 1, ""
+    for _ in range(args.steps):
+        v, rows, dt, threads, desc = oracle_sample(args.workload, per_step, x)
+        vals.append(v)
+        secs += dt
+        rows_tot += rows
+    value = float(np.mean(vals))
+    flops_step = causal_flops(w, x.key_len)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": flops_step / (value * 1e12) * 1e3 if value > 0 else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, bf16-rounded)",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "sample": "bounded random query rows per step (oracle on host cores)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- CUDA leg
+def our_arm(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    from exact_softmax_attention_fattn_gb300 import binding
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = dev_bf16(x.q), dev_bf16(x.k), dev_bf16(x.v)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    kl = None if x.key_len is None else torch.from_numpy(x.key_len).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = causal_flops(w, x.key_len)
+
+    def step():
+        binding.forward_into(q, k, v, o, lse, causal=w.causal, scale=w.softmax_scale, key_len=kl)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    st, detail = binding.last_error(stream)
+    if st != binding.FATTN_OK:
+        raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    st, detail = binding.last_error(stream)
+    if st != binding.FATTN_OK:
+        raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_total = float(sum(kernel_ms))
+    ms_max = ms_total
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        klh = None if x.key_len is None else torch.from_numpy(x.key_len)
+        for _ in range(2):
+            binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh)
+        n_e2e = max(3, min(args.steps, 10))
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            oh, lh = binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh)
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        h2d = 3 * q.numel() * 2 + (0 if klh is None else klh.numel() * 4)
+        d2h = oh.numel() * 2 + lh.numel() * 4
+        e2e = {"value": flops / e2e_s / 1e12 * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+
+    if rank != 0:
+        return
+    peak, peak_kind, _ = measured_peaks()
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    traffic = ncu_traffic(args.workload)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v_cpu, rows, dt, threads, desc = oracle_sample(args.workload, args.cpu_seconds, x)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, bf16-rounded)",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "key_padding": x.key_len is not None, "flops_per_step": flops,
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
+                     "traffic": traffic},
+        "pct_of_bf16_peak": 100.0 * achieved / peak,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "kernel": KERNEL_NAME,
+        "kernel_ms": {"min": min(kernel_ms), "median": float(np.median(kernel_ms)), "max": max(kernel_ms)},
+        "wall_s_timed_region": wall,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        our_arm(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+"""Thin ctypes binding over libfattn.so (include/fattn.h).
+
+Argument marshalling only: every step of the attention forward runs in the
+CUDA kernel behind `fattn_fwd`.  PyTorch supplies device memory and the
+current stream.  If the library is not built, or no GPU is present, calls
+raise FattnError: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "_lib", "libfattn.so")
+
+FATTN_OK = 0
+FATTN_ERR_INVALID_ARG = 1
+FATTN_ERR_UNSUPPORTED = 2
+FATTN_ERR_CUDA = 3
+FATTN_ERR_TIMEOUT = 4
+
+EXPORTED = ("fattn_fwd", "fattn_status_string", "fattn_last_error", "fattn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+_STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+                 4: "kernel wait timed out"}
+
+
+class FattnError(RuntimeError):
+    """A non-zero status from libfattn (the status code is in .status)."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS_NAMES.get(status, 'unknown status')} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfattn.so once; raise FattnError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise FattnError(FATTN_ERR_CUDA, f"{_LIB_PATH} is not built; run "
+                                 "`python -m exact_softmax_attention_fattn_gb300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.fattn_fwd.restype = ctypes.c_int
+            lib.fattn_fwd.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p,
+            ]
+            lib.fattn_status_string.restype = ctypes.c_char_p
+            lib.fattn_status_string.argtypes = [ctypes.c_int]
+            lib.fattn_last_error.restype = ctypes.c_int
+            lib.fattn_last_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+            lib.fattn_version.restype = ctypes.c_int
+            lib.fattn_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().fattn_status_string(int(status)).decode()
+
+
+def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, d: int,
+            scale: float, causal: bool, key_len_ptr: int | None, stream: int | None) -> int:
+    """fattn_fwd with raw addresses; returns the status code."""
+    return load_library().fattn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
+                                    float(scale), int(bool(causal)), key_len_ptr, stream)
+
+
+def last_error(stream=None) -> tuple[int, list[int]]:
+    """fattn_last_error on `stream` (a torch.cuda.Stream, a raw handle or None
+    for the current stream): (status, [status, role, barrier, unit])."""
+    import torch
+
+    if stream is None:
+        handle = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, int):
+        handle = stream
+    else:
+        handle = stream.cuda_stream
+    detail = (ctypes.c_int * 4)()
+    st = load_library().fattn_last_error(handle, detail)
+    return st, list(detail)
+
+
+def _check_qkv(q, k, v):
+    import torch
+
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be torch.bfloat16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share the shape [B, H, N, d]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+
+
+def forward_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None, key_len=None,
+                 stream=None) -> None:
+    """Run the kernel on device tensors, writing `o` (bf16 [B,H,N,d]) and `lse`
+    (fp32 [B,H,N]) in place; enqueued on `stream` (default: current stream)."""
+    import torch
+
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    kl_ptr = None
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or key_len.shape != (B,) or key_len.device != q.device:
+            raise ValueError("key_len must be an int32 tensor [B] on q's device")
+        kl_ptr = key_len.data_ptr()
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q.device):
+        handle = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+        st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
+                     causal, kl_ptr, handle)
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_fwd")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=None):
+    """O, LSE = attention forward of bf16 [B, H, N, d] tensors.
+
+    Device tensors: the kernel is enqueued on the current stream and the call
+    returns without synchronising.  Host tensors (pinned for speed): they are
+    copied to the current CUDA device, the kernel runs there, and O and LSE
+    are copied back (the call then synchronises).
+    `key_len` may be a tensor, a sequence of ints or None.
+    """
+    import torch
+
+    on_host = q.device.type == "cpu"
+    if on_host:
+        if not torch.cuda.is_available():
+            raise FattnError(FATTN_ERR_CUDA, "no CUDA device")
+        dev = torch.device("cuda", torch.cuda.current_device())
+        qd = q.to(dev, non_blocking=True)
+        kd = k.to(dev, non_blocking=True)
+        vd = v.to(dev, non_blocking=True)
+    else:
+        dev, qd, kd, vd = q.device, q, k, v
+    _check_qkv(qd, kd, vd)
+    kl = None
+    if key_len is not None:
+        kl = torch.as_tensor(key_len, dtype=torch.int32).to(dev, non_blocking=True).contiguous()
+    B, H, N, _ = qd.shape
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    forward_into(qd, kd, vd, o, lse, causal=causal, scale=scale, key_len=kl)
+    if on_host:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+        return o_h, l_h
+    return o, lse

@@ -1,0 +1,244 @@
+// C ABI of libfattn: argument validation, TMA tensor-map encoding and the
+// launch of the sm_103a attention kernel.  See include/fattn.h for the
+// contract of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fattn.h"
+#include "fattn_kernel.cuh"
+#include "v_prepass.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int* err = nullptr;             // int[4] device workspace
+  cudaMemPool_t pool = nullptr;   // private stream-ordered pool for per-call scratch
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+unsigned long long g_wait_limit_ns = 0;
+
+unsigned long long wait_limit_ns() {
+  if (g_wait_limit_ns == 0) {
+    unsigned long long ms = 2000;
+    if (const char* e = std::getenv("FATTN_WAIT_LIMIT_MS")) {
+      long long v = std::atoll(e);
+      if (v > 0) ms = (unsigned long long)v;
+    }
+    g_wait_limit_ns = ms * 1000000ull;
+  }
+  return g_wait_limit_ns;
+}
+
+// Sets the kernel's shared-memory limit and checks that it was compiled with
+// the register count its setmaxnreg split assumes (a split larger than the
+// launch allocation would never be granted).
+template <int D>
+int configure_kernel() {
+  cudaError_t e = cudaFuncSetAttribute(fattn::fattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)fattn::Cfg<D>::SMEM_BYTES);
+  if (e != cudaSuccess) return FATTN_ERR_CUDA;
+  cudaFuncAttributes a;
+  if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D>) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (a.numRegs != fattn::LAUNCH_REGS) return FATTN_ERR_UNSUPPORTED;
+  return FATTN_OK;
+}
+
+// A pool that keeps its memory (release threshold = max) so the per-call
+// scratch is recycled in stream order instead of returned to the driver.
+int make_pool(int dev, cudaMemPool_t* pool) {
+  cudaMemPoolProps props = {};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.handleTypes = cudaMemHandleTypeNone;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  if (cudaMemPoolCreate(pool, &props) != cudaSuccess) return FATTN_ERR_CUDA;
+  uint64_t keep = UINT64_MAX;
+  if (cudaMemPoolSetAttribute(*pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) return FATTN_ERR_CUDA;
+  return FATTN_OK;
+}
+
+// Per-device set-up, once: SM count, kernel attributes, the error word.
+int device_state(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  int rc = FATTN_OK;
+  if (!s.ready) {
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FATTN_ERR_CUDA;
+    rc = configure_kernel<64>();
+    if (rc == FATTN_OK) rc = configure_kernel<128>();
+    if (rc != FATTN_OK) return rc;
+    if (make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
+    if (cudaMalloc(&s.err, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (cudaMemset(s.err, 0, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FATTN_ERR_CUDA;
+    s.ready = true;
+  }
+  *out = &s;
+  return FATTN_OK;
+}
+
+bool is_device_pointer(const void* ptr) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// [B*H, N, d] 16-bit elements viewed as a 3-D tensor: x = head dim (innermost),
+// y = row, z = batch*head.  Boxes of 64 x 128 x 1 with 128-byte swizzle; rows
+// past N read as zero.
+int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType type) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2ull, (cuuint64_t)N * (cuuint64_t)d * 2ull};
+  cuuint32_t box[3] = {64u, 128u, 1u};
+  cuuint32_t elem[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, type, 3, const_cast<void*>(ptr), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Scratch of one call: V in its per-tile storage type, then one mode byte per tile.
+size_t scratch_bytes(int BH, int N, int D, int n_tiles) {
+  return round_up((size_t)BH * (size_t)N * (size_t)D * 2u, 256) + round_up((size_t)BH * (size_t)n_tiles, 256);
+}
+
+// Enqueues the V pre-pass and the attention kernel; `scratch` must hold scratch_bytes().
+template <int D>
+int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* scratch, int grid,
+            cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  uint8_t* v16 = reinterpret_cast<uint8_t*>(scratch);
+  uint8_t* modes = v16 + round_up((size_t)BH * (size_t)p.N * D * 2u, 256);
+  p.v_mode = modes;
+  CUtensorMap mq, mk, mv;
+  if (encode_map(&mq, q, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mv, v16, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) != FATTN_OK)
+    return FATTN_ERR_CUDA;
+  const long long prepass_blocks = (long long)BH * p.n_kv_tiles;
+  fattn::fattn_v_prepass_kernel<D><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+      reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.n_kv_tiles);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  fattn::fattn_fwd_kernel<D><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+}  // namespace
+
+extern "C" FATTN_API int fattn_version(void) { return 100; }
+
+extern "C" FATTN_API const char* fattn_status_string(int status) {
+  switch (status) {
+    case FATTN_OK: return "ok";
+    case FATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FATTN_ERR_CUDA: return "CUDA error";
+    case FATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                         int d, float scale, int causal, const int32_t* key_len, void* stream) {
+  // ---- synchronous argument checks: nothing is enqueued on failure
+  if (B < 0 || H < 0 || N < 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (key_len && !aligned(key_len, 4)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!is_device_pointer(q) || !is_device_pointer(k) || !is_device_pointer(v) || !is_device_pointer(o) ||
+      !is_device_pointer(lse) || (key_len && !is_device_pointer(key_len)))
+    return FATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  int rc = device_state(dev, &ds);
+  if (rc != FATTN_OK) return rc;
+
+  fattn::Params p;
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.key_len = key_len;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.n_qblocks = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
+  const long long units = (long long)B * H * p.n_qblocks;
+  if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  p.n_units = (int)units;
+  p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
+  if ((long long)B * H * p.n_kv_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  p.v_mode = nullptr;
+  p.wait_limit_ns = wait_limit_ns();
+  const int grid = (int)(units < ds->num_sms ? units : ds->num_sms);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  void* scratch = nullptr;
+  if (cudaMallocFromPoolAsync(&scratch, scratch_bytes(B * H, N, d, p.n_kv_tiles), ds->pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  rc = d == 64 ? enqueue<64>(q, k, v, p, scratch, grid, s) : enqueue<128>(q, k, v, p, scratch, grid, s);
+  if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
+  return rc;
+}
+
+extern "C" FATTN_API int fattn_last_error(void* stream, int* detail) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  int rc = device_state(dev, &ds);
+  if (rc != FATTN_OK) return rc;
+  int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, ds->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (detail)
+    for (int i = 0; i < 4; ++i) detail[i] = h[i];
+  if (h[0] != 0) {
+    if (cudaMemset(ds->err, 0, sizeof h) != cudaSuccess) return FATTN_ERR_CUDA;
+    return FATTN_ERR_TIMEOUT;
+  }
+  return FATTN_OK;
+}

@@ -1,0 +1,642 @@
+// Exact softmax attention forward, sm_103a: one fused, persistent kernel.
+//
+// What it computes ("understand-flashattention": forward-pass formulas,
+// numerically stable softmax, two-block online-softmax derivation, logsumexp
+// derivation; scale-then-mask order of "PyTorch profiling part 3: attention",
+// section "Naive attention"):
+//     O = softmax(mask(scale * Q K^T)) V,   LSE = rowwise log-sum-exp of the
+//     masked, scaled scores (natural log); an all-masked row gives O = 0 and
+//     LSE = -inf ("The safe softmax" section of the same profiling page).
+//
+// How (GB300 design, not the pages' Ampere blocking):
+//   * work unit = (batch*head, block of 2 x 128 query rows); CTAs are
+//     persistent and walk the units with a static stride, heaviest (latest,
+//     for causal) query blocks first;
+//   * warp 8 (one lane) is the TMA producer: Q tiles into two fixed buffers,
+//     K and V tiles into a STAGES-deep ring, all 128-byte swizzled panels of
+//     64 columns;
+//   * warp 9 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T (both operands in
+//     shared memory) and O_t += P_t V_j (P from tensor memory, V from shared
+//     memory), completion signalled with tcgen05.commit on mbarriers.  The two
+//     query tiles ping-pong: while one softmax group works on S_0, the tensor
+//     core runs the other tile's PV and S;
+//   * warps 0-3 and 4-7 are one softmax group per query tile, one thread per
+//     query row: the online-softmax step of the two-block derivation (running
+//     max m, normaliser l, rescaling of the unnormalised output by
+//     2^(m_old - m_new)), exponentials in base 2 with the scale folded in, P
+//     written back to tensor memory as bf16, then the final O / l and LSE.
+//     The rescale of O is skipped while the running max has grown by less
+//     than 2^8 since the last rescale: O and l keep a common, slightly stale
+//     reference, so the final O / l is unchanged (exact up to rounding).
+//   * every wait is bounded; on time-out the kernel records an error word,
+//     drains its own copies and MMAs, frees tensor memory and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <type_traits>
+
+#include "ptx.cuh"
+
+namespace fattn {
+
+constexpr int BM = 128;  // query rows per Q tile (TMEM lanes)
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int QT = 2;    // Q tiles per work unit
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;     // warps 10 and 11 complete the third warpgroup and idle
+constexpr int NUM_THREADS = 384;
+// Register split (setmaxnreg): the block launches with LAUNCH_REGS per thread
+// (ptxas' cap for 384 threads, one SM); the two softmax warpgroups grow to
+// SOFTMAX_REGS and the producer/MMA warpgroup shrinks to OTHER_REGS.  The
+// split uses exactly the launch allocation: 256*200 + 128*104 = 384*168.
+constexpr int LAUNCH_REGS = 168;
+constexpr int SOFTMAX_REGS = 200;
+constexpr int OTHER_REGS = 104;
+static_assert(256 * SOFTMAX_REGS + 128 * OTHER_REGS <= NUM_THREADS * LAUNCH_REGS, "register split exceeds launch");
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_S0 = 0;    // S_t at column 128*t, P_t packed into its first 64 columns
+constexpr uint32_t TMEM_O0 = 256;  // O_t at column 256 + 128*t
+constexpr float RESCALE_LOG2_THRESHOLD = 8.0f;
+constexpr uint32_t PANEL_BYTES = 128 * 128;  // 128 rows x 128 bytes (64 bf16 columns)
+
+// Storage type of one 128-row V tile in the pre-converted V buffer.
+enum : int { VMODE_F16 = 0, VMODE_BF16 = 1 };
+
+// Error word layout (int[4]): [0] status (0 ok, 4 timed out), [1] role,
+// [2] barrier id, [3] work unit.
+enum : int { ERR_TIMEOUT = 4 };
+enum : int { ROLE_SOFTMAX = 1, ROLE_PRODUCER = 2, ROLE_MMA = 3 };
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  const int32_t* key_len;  // [B] or nullptr
+  const uint8_t* v_mode;   // [B*H, n_kv_tiles]: storage type of each V tile (VMODE_*)
+  int* err;                // int[4]
+  int B, H, N;
+  float scale;       // softmax scale (natural units), >= 0
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  int n_qblocks;  // ceil(N / 256)
+  int n_units;    // B * H * n_qblocks
+  int n_kv_tiles; // ceil(N / 128)
+  unsigned long long wait_limit_ns;
+};
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t TILE_BYTES = BM * D * 2;  // one Q, K or V tile (BN == BM)
+  static constexpr int STAGES = D == 128 ? 5 : 8;
+  static constexpr uint32_t Q_OFF = 0;
+  static constexpr uint32_t RING_OFF = QT * TILE_BYTES;
+  static constexpr uint32_t BAR_OFF = RING_OFF + STAGES * TILE_BYTES;
+  // barrier ids
+  static constexpr int B_Q_FULL = 0;                     // [2]
+  static constexpr int B_Q_EMPTY = 2;                    // [2]
+  static constexpr int B_S_FULL = 4;                     // [2]
+  static constexpr int B_P_FULL = 6;                     // [2]
+  static constexpr int B_O_FULL = 8;                     // [2]
+  static constexpr int B_O_EMPTY = 10;                   // [2]
+  static constexpr int B_DRAIN = 12;                     // [1]
+  static constexpr int B_KV_FULL = 13;                   // [STAGES]
+  static constexpr int B_KV_EMPTY = 13 + STAGES;         // [STAGES]
+  static constexpr int NUM_BARS = 13 + 2 * STAGES;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
+  static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
+  static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+};
+
+// ------------------------------------------------------------------ descriptors
+// Shared-memory matrix descriptor (tcgen05 "matrix descriptor"): start address,
+// leading- and stride-dimension byte offsets (all >> 4), descriptor version 1,
+// layout 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: D fp32; A and B both bf16 or both
+// f16; shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool ab_bf16, bool b_mn_major) {
+  return (1u << 4)                          // D format f32
+         | ((ab_bf16 ? 1u : 0u) << 7)      // A format: 0 f16, 1 bf16
+         | ((ab_bf16 ? 1u : 0u) << 10)     // B format: same as A
+         | (0u << 15)                       // A K-major
+         | ((b_mn_major ? 1u : 0u) << 16)
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ work units
+struct Unit {
+  int bh, b, r0;
+  int n0, n1;              // K/V tiles Q tile 0 / 1 visits (0: nothing to do)
+  int min_lim0, min_lim1;  // smallest per-row key limit in each tile
+  int kl;                  // effective key length of this batch entry
+  int nkv;                 // max(n0, n1)
+  bool valid0, valid1;     // tile has at least one row < N
+  __device__ __forceinline__ int n(int t) const { return t ? n1 : n0; }
+  __device__ __forceinline__ int min_lim(int t) const { return t ? min_lim1 : min_lim0; }
+  __device__ __forceinline__ bool valid(int t) const { return t ? valid1 : valid0; }
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+  Unit w;
+  const int BH = p.B * p.H;
+  const int round = u / BH;
+  w.bh = u % BH;
+  w.b = w.bh / p.H;
+  const int qb = p.n_qblocks - 1 - round;  // latest (heaviest under causal) blocks first
+  w.r0 = qb * (QT * BM);
+  int kl = p.N;
+  if (p.key_len) {
+    kl = __ldg(p.key_len + w.b);
+    kl = kl < 0 ? 0 : (kl > p.N ? p.N : kl);
+  }
+  w.kl = kl;
+  int nn[QT], ml[QT];
+  bool vv[QT];
+#pragma unroll
+  for (int t = 0; t < QT; ++t) {
+    const int row0 = w.r0 + t * BM;
+    vv[t] = row0 < p.N;
+    int max_lim = kl;
+    int min_lim = kl;
+    if (p.causal) {
+      max_lim = min(kl, row0 + BM);
+      min_lim = min(kl, row0 + 1);
+    }
+    nn[t] = (vv[t] && max_lim > 0) ? (max_lim + BN - 1) / BN : 0;
+    ml[t] = min_lim;
+  }
+  w.n0 = nn[0];
+  w.n1 = nn[1];
+  w.min_lim0 = ml[0];
+  w.min_lim1 = ml[1];
+  w.valid0 = vv[0];
+  w.valid1 = vv[1];
+  w.nkv = max(w.n0, w.n1);
+  return w;
+}
+
+// Persistent schedule: CTA c takes, in round r, unit r*G + c (r even) or
+// r*G + G-1-c (r odd).  Units are ordered heaviest first, so the snake pairs
+// heavy and light units on each CTA.
+__device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
+
+// ------------------------------------------------------------------ bounded wait
+struct Waiter {
+  volatile int* abort_flag;  // shared memory
+  int* err;
+  unsigned long long limit_ns;
+  int role;
+};
+
+// Returns false (and raises the CTA's abort flag) if the wait gave up.
+__device__ __forceinline__ bool wait_slow(const Waiter& w, uint32_t bar, uint32_t parity, int bar_id, int unit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      *w.abort_flag = 1;
+      if (atomicCAS(w.err, 0, ERR_TIMEOUT) == 0) {
+        w.err[1] = w.role;
+        w.err[2] = bar_id;
+        w.err[3] = unit;
+      }
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(const Waiter& w, uint32_t bar, uint32_t parity, int bar_id, int unit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(w, bar, parity, bar_id, unit);
+}
+
+// Bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < limit_ns) {
+  }
+}
+
+template <int T>
+using TileC = std::integral_constant<int, T>;
+
+// ------------------------------------------------------------------ the kernel
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fattn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  auto bar = [&](int id) -> uint32_t { return base + C::BAR_OFF + 8u * (uint32_t)id; };
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int t = 0; t < QT; ++t) {
+      mbar_init(bar(C::B_Q_FULL + t), 1);
+      mbar_init(bar(C::B_Q_EMPTY + t), 1);
+      mbar_init(bar(C::B_S_FULL + t), 1);
+      mbar_init(bar(C::B_P_FULL + t), BM);
+      mbar_init(bar(C::B_O_FULL + t), 1);
+      mbar_init(bar(C::B_O_EMPTY + t), BM);
+    }
+    mbar_init(bar(C::B_DRAIN), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(C::B_KV_FULL + s), 1);
+      mbar_init(bar(C::B_KV_EMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(base + C::MISC_OFF, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_slot;
+
+  Waiter waiter{abort_flag, p.err, p.wait_limit_ns, 0};
+
+  if (warp >= 8) {
+  regs_shrink<OTHER_REGS>();
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      waiter.role = ROLE_PRODUCER;
+      uint32_t g = 0;                 // K/V tiles issued so far (ring position)
+      uint32_t q_use0 = 0, q_use1 = 0;  // Q tiles issued so far, per buffer
+      bool ok = true;
+      auto load_q = [&](auto tc, const Unit& w, int u, uint32_t& q_use) {
+        constexpr int t = decltype(tc)::value;
+        if (!ok || w.n(t) == 0) return;
+        ok = wait_bar(waiter, bar(C::B_Q_EMPTY + t), (q_use & 1u) ^ 1u, C::B_Q_EMPTY + t, u);
+        if (!ok) return;
+        mbar_arrive_expect_tx(bar(C::B_Q_FULL + t), C::TILE_BYTES);
+        const uint32_t dst = base + C::Q_OFF + (uint32_t)t * C::TILE_BYTES;
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_3d(dst + pn * PANEL_BYTES, &tmap_q, bar(C::B_Q_FULL + t), 64 * pn, w.r0 + t * BM, w.bh);
+        ++q_use;
+      };
+      for (int r = 0; ok && r * G < p.n_units; ++r) {
+        const int u = unit_of(r, cta, G);
+        if (u >= p.n_units) continue;
+        const Unit w = decode_unit(p, u);
+        load_q(TileC<0>{}, w, u, q_use0);
+        load_q(TileC<1>{}, w, u, q_use1);
+        for (int j = 0; ok && j < w.nkv; ++j) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t slot = g % C::STAGES;
+            const uint32_t ph = (g / C::STAGES) & 1u;
+            ok = wait_bar(waiter, bar(C::B_KV_EMPTY + slot), ph ^ 1u, C::B_KV_EMPTY + slot, u);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(C::B_KV_FULL + slot), C::TILE_BYTES);
+            const uint32_t dst = base + C::RING_OFF + slot * C::TILE_BYTES;
+            const CUtensorMap* map = which == 0 ? &tmap_k : &tmap_v;
+#pragma unroll
+            for (int pn = 0; pn < C::PANELS; ++pn)
+              tma_load_3d(dst + pn * PANEL_BYTES, map, bar(C::B_KV_FULL + slot), 64 * pn, j * BN, w.bh);
+            ++g;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) for every copy that may still be in flight.
+        const uint32_t first = g > (uint32_t)C::STAGES ? g - C::STAGES : 0u;
+        for (uint32_t gi = first; gi < g; ++gi)
+          drain_wait(bar(C::B_KV_FULL + gi % C::STAGES), (gi / C::STAGES) & 1u, 20000000ull);
+        if (q_use0) drain_wait(bar(C::B_Q_FULL + 0), (q_use0 - 1) & 1u, 20000000ull);
+        if (q_use1) drain_wait(bar(C::B_Q_FULL + 1), (q_use1 - 1) & 1u, 20000000ull);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      waiter.role = ROLE_MMA;
+      constexpr uint32_t IDESC_S = idesc_f16kind(BM, BN, true, false);      // Q, K bf16
+      constexpr uint32_t IDESC_PV_F16 = idesc_f16kind(BM, D, false, true);  // P, V f16; V MN-major
+      constexpr uint32_t IDESC_PV_BF16 = idesc_f16kind(BM, D, true, true);  // P, V bf16; V MN-major
+      uint32_t g = 0;  // ring position consumed
+      uint32_t q_use[QT] = {0, 0};
+      uint32_t units_done[QT] = {0, 0};
+      uint32_t pv_cnt[QT] = {0, 0};
+      bool ok = true;
+      bool issued_any = false;
+
+      // S_t = Q_t K^T from the K tile in `slot`.
+      auto issue_s = [&](auto tc, uint32_t slot) {
+        constexpr int t = decltype(tc)::value;
+        const uint32_t qa = base + C::Q_OFF + (uint32_t)t * C::TILE_BYTES;
+        const uint32_t ka = base + C::RING_OFF + slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk / 4) * PANEL_BYTES + (uint32_t)(kk % 4) * 32u;
+          mma_ss(tmem + TMEM_S0 + 128u * t, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_t V with P in tensor memory, V (keys x D, D contiguous) in `slot`.
+      auto issue_pv = [&](auto tc, uint32_t slot, bool accumulate, uint32_t idesc_pv) {
+        constexpr int t = decltype(tc)::value;
+        const uint32_t va = base + C::RING_OFF + slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_ts(tmem + TMEM_O0 + 128u * t, tmem + TMEM_S0 + 128u * t + 8u * kk,
+                 smem_desc(va + (uint32_t)kk * 2048u, PANEL_BYTES, 1024), idesc_pv,
+                 (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int r = 0; ok && r * G < p.n_units; ++r) {
+        const int u = unit_of(r, cta, G);
+        if (u >= p.n_units) continue;
+        const Unit w = decode_unit(p, u);
+        if (w.nkv == 0) continue;
+        auto kslot = [&](int j) { return (g + 2u * j) % C::STAGES; };
+        auto kphase = [&](int j) { return ((g + 2u * j) / C::STAGES) & 1u; };
+        auto vslot = [&](int j) { return (g + 2u * j + 1u) % C::STAGES; };
+        auto vphase = [&](int j) { return ((g + 2u * j + 1u) / C::STAGES) & 1u; };
+
+        // prologue: S_t,0 for each tile with work
+        ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(0)), kphase(0), C::B_KV_FULL + kslot(0), u);
+        auto prologue = [&](auto tc) {
+          constexpr int t = decltype(tc)::value;
+          if (!ok || w.n(t) == 0) return;
+          ok = wait_bar(waiter, bar(C::B_Q_FULL + t), q_use[t] & 1u, C::B_Q_FULL + t, u);
+          if (!ok) return;
+          ++q_use[t];
+          tc_fence_after();
+          issue_s(tc, kslot(0));
+          mma_commit(bar(C::B_S_FULL + t));
+          if (w.n(t) == 1) mma_commit(bar(C::B_Q_EMPTY + t));
+        };
+        prologue(TileC<0>{});
+        prologue(TileC<1>{});
+        if (!ok) break;
+        mma_commit(bar(C::B_KV_EMPTY + kslot(0)));
+        issued_any = true;
+
+        const uint8_t* modes = p.v_mode + (size_t)w.bh * p.n_kv_tiles;
+        int vmode_next = __ldg(modes);
+        for (int j = 0; ok && j < w.nkv; ++j) {
+          const uint32_t idesc_pv = vmode_next == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
+          if (j + 1 < w.nkv) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+          ok = wait_bar(waiter, bar(C::B_KV_FULL + vslot(j)), vphase(j), C::B_KV_FULL + vslot(j), u);
+          // O_t += P_t V_j, then S_t,j+1 = Q_t K_j+1^T (tile 1's MMAs run while tile 0's softmax works)
+          auto step = [&](auto tc) {
+            constexpr int t = decltype(tc)::value;
+            if (!ok || j >= w.n(t)) return;
+            if (j == 0) {
+              ok = wait_bar(waiter, bar(C::B_O_EMPTY + t), (units_done[t] & 1u) ^ 1u, C::B_O_EMPTY + t, u);
+              if (!ok) return;
+            }
+            ok = wait_bar(waiter, bar(C::B_P_FULL + t), pv_cnt[t] & 1u, C::B_P_FULL + t, u);
+            if (!ok) return;
+            ++pv_cnt[t];
+            tc_fence_after();
+            issue_pv(tc, vslot(j), j > 0, idesc_pv);
+            if (j == w.n(t) - 1) mma_commit(bar(C::B_O_FULL + t));
+            if (j + 1 < w.n(t)) {
+              ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(j + 1)), kphase(j + 1), C::B_KV_FULL + kslot(j + 1), u);
+              if (!ok) return;
+              tc_fence_after();
+              issue_s(tc, kslot(j + 1));
+              mma_commit(bar(C::B_S_FULL + t));
+              if (j + 1 == w.n(t) - 1) mma_commit(bar(C::B_Q_EMPTY + t));
+            }
+          };
+          step(TileC<0>{});
+          step(TileC<1>{});
+          if (!ok) break;
+          mma_commit(bar(C::B_KV_EMPTY + vslot(j)));
+          if (j + 1 < w.nkv) mma_commit(bar(C::B_KV_EMPTY + kslot(j + 1)));
+        }
+        g += 2u * (uint32_t)w.nkv;
+        if (w.n0 > 0) ++units_done[0];
+        if (w.n1 > 0) ++units_done[1];
+      }
+      // Drain: every MMA this thread issued has completed before TMEM is freed.
+      if (issued_any) {
+        mma_commit(bar(C::B_DRAIN));
+        drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
+      }
+    }
+  }
+  } else {
+    regs_grow<SOFTMAX_REGS>();
+    // ------------------------------------------------------------ softmax groups
+    waiter.role = ROLE_SOFTMAX;
+    const int t = warp / 4;                  // query tile of this group
+    const int quarter = warp % 4;            // TMEM lane quarter
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + TMEM_S0 + 128u * t;
+    const uint32_t o_addr = tmem + lane_off + TMEM_O0 + 128u * t;
+    const uint32_t bar_s_full = bar(C::B_S_FULL + t);
+    const uint32_t bar_p_full = bar(C::B_P_FULL + t);
+    const uint32_t bar_o_full = bar(C::B_O_FULL + t);
+    const uint32_t bar_o_empty = bar(C::B_O_EMPTY + t);
+    const float c = p.scale_log2;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+
+    for (int r = 0; ok && r * G < p.n_units; ++r) {
+      const int u = unit_of(r, cta, G);
+      if (u >= p.n_units) continue;
+      const Unit w = decode_unit(p, u);
+      if (!w.valid(t)) continue;
+      const int n_t = w.n(t);
+      const int min_lim = w.min_lim(t);
+      const int row = w.r0 + t * BM + row_in_tile;
+      const bool row_ok = row < p.N;
+      const size_t row_flat = (size_t)w.bh * (size_t)p.N + (size_t)row;
+      if (n_t == 0) {
+        // no visible key at all: O = 0, LSE = -inf
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          p.lse[row_flat] = -INFINITY;
+        }
+        continue;
+      }
+      const int lim = p.causal ? min(w.kl, row + 1) : w.kl;  // keys [0, lim) are visible
+      float m_ref = -INFINITY;
+      float l = 0.0f;
+      const uint8_t* modes = p.v_mode + (size_t)w.bh * p.n_kv_tiles;
+      int vmode_next = __ldg(modes);
+
+      for (int j = 0; j < n_t; ++j) {
+        const int vmode = vmode_next;
+        if (j + 1 < n_t) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+        ok = wait_bar(waiter, bar_s_full, s_cnt & 1u, C::B_S_FULL + t, u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++s_cnt;
+        tc_fence_after();
+
+        float s[BN];
+        {
+          uint32_t r32[BN];
+          tmem_ld128(s_addr, r32);
+          tmem_ld_wait(r32);
+#pragma unroll
+          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r32[i]);
+        }
+        const bool masked_tile = (j + 1) * BN > min_lim;
+        const int vis_n = lim - j * BN;  // columns [0, vis_n) visible
+        if (masked_tile) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) s[i] = i < vis_n ? s[i] : -INFINITY;
+        }
+        // row max: 8 independent chains of 3-input max
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(s[i], s[i + 8], s[i + 16]);
+#pragma unroll
+        for (int i = 24; i < BN; i += 16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[i + k], i + 8 + k < BN ? s[i + 8 + k] : -INFINITY);
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        const float m_new = fmaxf(m_ref, mx);
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (m_ref == -INFINITY) {
+          m_ref = m_new;  // first visible scores: O is overwritten by this tile's PV
+        } else if ((m_new - m_ref) * c > RESCALE_LOG2_THRESHOLD) {
+          alpha = ex2((m_ref - m_new) * c);
+          m_ref = m_new;
+          rescale = true;
+        }
+        const float mc = (m_ref == -INFINITY) ? 0.0f : m_ref * c;
+
+        // p = 2^(s*c - m*c): kept in fp32 for l, rounded once for PV, to fp16
+        // when this V tile is stored in fp16 (the usual case: 11 significant
+        // bits) and to bf16 when it is not.  Masked entries are exactly zero.
+        float sum8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
+        uint32_t pk[BN / 2];
+        auto exp_pack = [&](auto pack) {
+#pragma unroll
+          for (int i = 0; i < BN; i += 2) {
+            float p0 = ex2(fmaf(s[i], c, -mc));
+            float p1 = ex2(fmaf(s[i + 1], c, -mc));
+            if (masked_tile) {
+              p0 = i < vis_n ? p0 : 0.0f;
+              p1 = i + 1 < vis_n ? p1 : 0.0f;
+            }
+            pk[i / 2] = pack(p0, p1);
+            sum8[(i / 2) % 8] += p0 + p1;
+          }
+        };
+        if (vmode == VMODE_F16)
+          exp_pack([](float a, float b) { return pack_f16x2(a, b); });
+        else
+          exp_pack([](float a, float b) { return pack_bf16x2(a, b); });
+        const float rs = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        l = l * alpha + rs;
+
+        // correction: rescale this row of O (PV of the previous tile has completed,
+        // since S of this tile was issued after it and has completed)
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r32[32];
+            tmem_ld32(o_addr + 32u * cc, r32);
+            tmem_ld_wait(r32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r32[i] = __float_as_uint(__uint_as_float(r32[i]) * alpha);
+            tmem_st32(o_addr + 32u * cc, r32);
+          }
+        }
+        // P over the first 64 columns of S
+        {
+          uint32_t r32[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r32[i] = pk[i];
+          tmem_st32(s_addr, r32);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r32[i] = pk[32 + i];
+          tmem_st32(s_addr + 32u, r32);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_p_full);
+      }
+      if (!ok) break;
+
+      // epilogue: O / l -> bf16, LSE = m*scale + ln(l)
+      ok = wait_bar(waiter, bar_o_full, o_cnt & 1u, C::B_O_FULL + t, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ++o_cnt;
+      tc_fence_after();
+      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r32[32];
+        tmem_ld32(o_addr + 32u * cc, r32);
+        tmem_ld_wait(r32);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D + 32 * cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r32[8 * i + 0]) * inv_l, __uint_as_float(r32[8 * i + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(r32[8 * i + 2]) * inv_l, __uint_as_float(r32[8 * i + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(r32[8 * i + 4]) * inv_l, __uint_as_float(r32[8 * i + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(r32[8 * i + 6]) * inv_l, __uint_as_float(r32[8 * i + 7]) * inv_l);
+            dst[i] = v;
+          }
+        }
+      }
+      if (row_ok) {
+        const float lse = (l > 0.0f) ? (m_ref * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[row_flat] = lse;
+      }
+      tc_fence_before();
+      mbar_arrive(bar_o_empty);
+    }
+  }
+
+  __syncwarp();  // the producer and MMA warps ran their roles on one lane
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == MMA_WARP) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace fattn

@@ -1,0 +1,80 @@
+// V pre-pass: stores every 128-row tile of V in the type its P V product
+// will use.
+//
+// The attention kernel rounds the probabilities P once, to the operand type
+// of the P V tensor-core product, and tcgen05 kind::f16 takes A and B of the
+// same type.  fp16 keeps 11 significant bits of P against bf16's 8, which is
+// what keeps the bf16 output within the stated error on peaky softmax rows.
+// So each tile whose largest |v| lies in [2^-8, 65504] (fp16 then holds every
+// element to fp16 precision without overflow) is converted to fp16; any
+// other tile (huge or tiny values, inf) keeps its bf16 bits and its P is
+// rounded to bf16.  The per-tile choice is written to `mode`.
+//
+// HBM-bound: one read of V, one write of the same number of bytes.
+#pragma once
+
+#include <cstdint>
+
+#include "fattn_kernel.cuh"
+
+namespace fattn {
+
+constexpr int PREPASS_THREADS = 256;
+
+template <int D>
+__global__ void __launch_bounds__(PREPASS_THREADS)
+    fattn_v_prepass_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, uint8_t* __restrict__ mode, int N,
+                           int n_tiles) {
+  constexpr int VEC = 8;                                  // bf16 per 16-byte vector
+  constexpr int PER = BN * D / VEC / PREPASS_THREADS;     // vectors per thread
+  const long long tile_id = blockIdx.x;
+  const int tile = (int)(tile_id % n_tiles);
+  const long long bh = tile_id / n_tiles;
+  const int row0 = tile * BN;
+  const int rows = min(BN, N - row0);
+  const int nvec = rows * D / VEC;
+  const size_t base = ((size_t)bh * (size_t)N + (size_t)row0) * (D / VEC);
+
+  uint4 buf[PER];
+  float mx = 0.0f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int idx = threadIdx.x + i * PREPASS_THREADS;
+    if (idx < nvec) {
+      buf[i] = __ldg(v + base + idx);
+      const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mx = fmaxf(mx, fabsf(__uint_as_float(w[k] << 16)));
+        mx = fmaxf(mx, fabsf(__uint_as_float(w[k] & 0xFFFF0000u)));
+      }
+    }
+  }
+  __shared__ float warp_max[PREPASS_THREADS / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (threadIdx.x % 32 == 0) warp_max[threadIdx.x / 32] = mx;
+  __syncthreads();
+  mx = warp_max[0];
+#pragma unroll
+  for (int i = 1; i < PREPASS_THREADS / 32; ++i) mx = fmaxf(mx, warp_max[i]);
+  const bool to_f16 = mx >= 0.00390625f && mx <= 65504.0f;
+
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int idx = threadIdx.x + i * PREPASS_THREADS;
+    if (idx < nvec) {
+      uint4 o = buf[i];
+      if (to_f16) {
+        o.x = pack_f16x2(__uint_as_float(buf[i].x << 16), __uint_as_float(buf[i].x & 0xFFFF0000u));
+        o.y = pack_f16x2(__uint_as_float(buf[i].y << 16), __uint_as_float(buf[i].y & 0xFFFF0000u));
+        o.z = pack_f16x2(__uint_as_float(buf[i].z << 16), __uint_as_float(buf[i].z & 0xFFFF0000u));
+        o.w = pack_f16x2(__uint_as_float(buf[i].w << 16), __uint_as_float(buf[i].w & 0xFFFF0000u));
+      }
+      v16[base + idx] = o;
+    }
+  }
+  if (threadIdx.x == 0) mode[bh * n_tiles + tile] = to_f16 ? VMODE_F16 : VMODE_BF16;
+}
+
+}  // namespace fattn

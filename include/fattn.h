@@ -1,0 +1,111 @@
+/*
+ * fattn: exact softmax attention forward on GB300 (sm_103a), C ABI.
+ *
+ * The operation ("understand-flashattention", forward-pass formulas and the
+ * logsumexp derivation; scale-then-mask order and the -inf mask of "PyTorch
+ * profiling part 3: attention", section "Naive attention"):
+ *
+ *     S   = scale * Q K^T                 per (batch b, head h), N x N
+ *     S'  = S with masked entries = -inf  (causal: key j visible to query i
+ *                                          iff j <= i; key padding: key j
+ *                                          visible iff j < key_len[b]; both
+ *                                          masks combine with AND)
+ *     O   = softmax(S') V                 row-wise softmax
+ *     LSE = log(sum_j exp(S'_ij))         natural log, per query row
+ *
+ * computed tile by tile with the online-softmax recurrence (running max,
+ * normaliser and rescaled partial output, normalised once at the end: the
+ * two-block derivation of "understand-flashattention").  A row with no
+ * visible key returns O = 0 and LSE = -inf (the safe-softmax convention of
+ * the profiling page, section "The safe softmax").
+ *
+ * All entry points are plain C; tensors are raw pointers.  There is no CPU
+ * fallback: every result comes from the CUDA kernel.
+ */
+#ifndef FATTN_H_
+#define FATTN_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FATTN_API __attribute__((visibility("default")))
+#else
+#define FATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+  FATTN_OK = 0,
+  FATTN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or scale is invalid */
+  FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration this build runs (head dim) */
+  FATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  FATTN_ERR_TIMEOUT = 4      /* a bounded wait inside the kernel gave up (see fattn_last_error) */
+} fattn_status;
+
+/*
+ * fattn_fwd: O = softmax(mask(scale * Q K^T)) V and the row log-sum-exp.
+ *
+ *   q, k, v  device pointers, bf16, [B, H, N, d] contiguous (head dim
+ *            innermost, as "PyTorch profiling part 3: attention" lays out
+ *            q, k, v: [batch, heads, seq, head_dim]); 16-byte aligned.
+ *   o        device pointer, bf16, [B, H, N, d] contiguous, written; 16-byte aligned.
+ *   lse      device pointer, fp32, [B, H, N] contiguous, written (natural log).
+ *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 0.
+ *            If B*H*N == 0 the call does nothing and returns FATTN_OK.
+ *   d        head dim: 64 or 128 (others return FATTN_ERR_UNSUPPORTED).
+ *   scale    softmax scale applied to Q K^T before the mask; finite and >= 0
+ *            (usually 1/sqrt(d)).
+ *   causal   nonzero: key j is visible to query i only if j <= i.
+ *   key_len  device pointer to int32[B] or NULL (all N keys).  Keys
+ *            j >= key_len[b] are masked for batch entry b; values are
+ *            clamped to [0, N].  Query rows are never masked.
+ *   stream   a cudaStream_t (NULL = legacy default stream).
+ *
+ * Ownership: the caller allocates and owns every tensor; the library keeps
+ * no reference after the call returns.  The library owns a 16-byte error
+ * word per device and a private stream-ordered memory pool per device (both
+ * created on first use, kept until process exit).  Each call takes
+ * B*H*N*d*2 bytes (+ one byte per 128-row V tile) of scratch from that pool
+ * on `stream` and returns it in stream order after its kernels: V stored in
+ * the operand type of the P V product (fp16 per 128-row tile where V's
+ * range allows, else bf16), so the probabilities P are rounded to fp16.
+ *
+ * Asynchrony: the call validates its arguments synchronously, then enqueues
+ * two kernels on `stream` (the V pre-pass and the attention kernel) and
+ * returns without synchronising.  Time-outs of the kernel's bounded waits
+ * are reported later by fattn_last_error().
+ *
+ * Returns FATTN_OK, FATTN_ERR_INVALID_ARG (null pointer with B*H*N > 0,
+ * negative size, misaligned pointer, host pointer, non-finite or negative
+ * scale, sizes beyond int32 index space), FATTN_ERR_UNSUPPORTED (d not 64 or
+ * 128) or FATTN_ERR_CUDA (launch failed; no kernel ran).  Argument errors
+ * are detected before anything is enqueued.
+ */
+FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+              int d, float scale, int causal, const int32_t* key_len, void* stream);
+
+/* A static, human-readable name for a status code. */
+FATTN_API const char* fattn_status_string(int status);
+
+/*
+ * Synchronises `stream` and reports whether any fattn kernel on the current
+ * device timed out in a bounded wait since the last call: FATTN_ERR_TIMEOUT
+ * (and clears the flag), FATTN_ERR_CUDA if the synchronisation failed, else
+ * FATTN_OK.  If detail is not NULL it receives 4 ints: status, role
+ * (1 softmax, 2 TMA producer, 3 MMA issuer), barrier id and work unit of the
+ * first time-out.
+ */
+FATTN_API int fattn_last_error(void* stream, int* detail);
+
+/* Library version, major*10000 + minor*100 + patch. */
+FATTN_API int fattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H_ */

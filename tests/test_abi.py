@@ -1,0 +1,138 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every
+symbol include/fattn.h declares, and rejects bad arguments before touching
+the device."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from exact_softmax_attention_fattn_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_symbols() -> list[str]:
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"FATTN_API\s+[\w\s\*]+?\b(fattn_\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_boundary():
+    assert set(declared_symbols()) >= {"fattn_fwd", "fattn_status_string", "fattn_last_error", "fattn_version"}
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_no_torch_in_the_boundary():
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        assert "torch" not in text.lower().replace("pytorch", "")
+        assert "#include <cuda" not in text
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "ok"
+    assert binding.status_string(1) == "invalid argument"
+    assert binding.status_string(2) == "unsupported configuration"
+    assert binding.status_string(3) == "CUDA error"
+    assert binding.status_string(4) == "kernel wait timed out"
+    assert binding.status_string(99) == "unknown status"
+    assert lib.fattn_version() >= 100
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: each call below fails validation first
+
+
+def call(B=1, H=1, N=128, d=64, scale=0.125, causal=0, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, kl=None):
+    return binding.fwd_raw(q, k, v, o, lse, B, H, N, d, scale, causal, kl, None)
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert call(B=0) == binding.FATTN_OK
+    assert call(N=0, q=0, k=0, v=0, o=0, lse=0) == binding.FATTN_OK
+    assert call(H=0, d=96) == binding.FATTN_OK
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(H=-2), dict(N=-5)])
+def test_negative_sizes(lib, kw):
+    assert call(**kw) == binding.FATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("scale", [math.nan, math.inf, -math.inf, -0.5])
+def test_bad_scale(lib, scale):
+    assert call(scale=scale) == binding.FATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o", "lse"])
+def test_null_pointer(lib, which):
+    assert call(**{which: 0}) == binding.FATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [0, 16, 32, 96, 127, 256])
+def test_unsupported_head_dim(lib, d):
+    assert call(d=d) == binding.FATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v", "o"])
+def test_misaligned_tensor(lib, which):
+    assert call(**{which: FAKE + 8}) == binding.FATTN_ERR_INVALID_ARG
+
+
+def test_misaligned_lse_and_key_len(lib):
+    assert call(lse=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
+    assert call(kl=FAKE + 1) == binding.FATTN_ERR_INVALID_ARG
+
+
+def test_index_space_overflow(lib):
+    assert call(B=1 << 16, H=1 << 16) == binding.FATTN_ERR_INVALID_ARG
+    assert call(N=0x7FFFFFFF) == binding.FATTN_ERR_INVALID_ARG
+
+
+def test_host_pointer_rejected(lib):
+    buf = np.zeros(128 * 64 * 4, dtype=np.uint8)
+    addr = buf.ctypes.data
+    addr += (-addr) % 16
+    assert call(q=addr, k=addr, v=addr, o=addr, lse=addr) == binding.FATTN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "libfattn.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(binding.FattnError):
+        binding.load_library()
+
+
+def test_last_error_without_gpu(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("checks the no-GPU path")
+    detail = (ctypes.c_int * 4)()
+    assert lib.fattn_last_error(None, detail) == binding.FATTN_ERR_CUDA
+
+
+def test_forward_without_gpu_raises():
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("checks the no-GPU path")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(binding.FattnError):
+        binding.forward(q, q, q)
