@@ -48,12 +48,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 CSRC = os.path.join(ROOT, "exact_softmax_attention_fattn_gb300", "csrc")
 
 
+KERNEL_SOURCES = ("fattn_kernel.cuh", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the attention kernel's own source (not the host launcher)."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -319,7 +322,7 @@ def our_arm(args, rank: int, world: int, local_rank: int):
         "pct_of_bf16_peak": 100.0 * achieved / peak,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,  # V pre-pass + attention kernel per step
         "kernel": KERNEL_NAME,
         "kernel_ms": {"min": min(kernel_ms), "median": float(np.median(kernel_ms)), "max": max(kernel_ms)},
         "wall_s_timed_region": wall,
