@@ -242,3 +242,119 @@ extern "C" FATTN_API int fattn_last_error(void* stream, int* detail) {
   }
   return FATTN_OK;
 }
+
+// ------------------------------------------------------------------------
+// fattn_fwd_noalloc: the same forward for callers that cannot allocate
+// device memory.  Its scratch (the V copy in the P V operand type, the
+// per-tile storage modes and a 16-byte error word) lives in one static
+// device array, fixed at build time, instead of a pool allocation.
+namespace {
+
+constexpr size_t kNoAllocScratch = FATTN_NOALLOC_SCRATCH_BYTES;  // V copy + tile modes
+constexpr size_t kNoAllocErrWord = 256;                          // error word after them
+
+}  // namespace
+
+// Device scratch of the no-allocation entry point.  In host code this name is
+// only a stand-in for the symbol: its device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratch + kNoAllocErrWord];
+
+namespace {
+
+struct NoAllocState {
+  bool ready = false;
+  int num_sms = 0;
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+
+std::mutex g_noalloc_mu;
+NoAllocState g_noalloc[kMaxDevices];
+
+// Per-device set-up with `dev` current: kernel attributes, SM count, the
+// tensor-map encoder and the scratch symbol's device address.  Allocates nothing.
+int noalloc_state(int dev, NoAllocState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocState& s = g_noalloc[dev];
+  if (!s.ready) {
+    {
+      std::lock_guard<std::mutex> enc_lock(g_mu);
+      if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return FATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FATTN_ERR_CUDA;
+    int rc = configure_kernel<64>();
+    if (rc == FATTN_OK) rc = configure_kernel<128>();
+    if (rc != FATTN_OK) return rc;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return FATTN_ERR_CUDA;
+    }
+    s.scratch = reinterpret_cast<uint8_t*>(ptr);
+    s.ready = true;
+  }
+  *out = &s;
+  return FATTN_OK;
+}
+
+}  // namespace
+
+extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                           int H, int N, int d, float scale, int causal, const int32_t* key_len,
+                                           void* stream) {
+  if (B < 0 || H < 0 || N < 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
+  const int n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
+  if ((long long)B * H * n_kv_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  // the static scratch bounds the problem size
+  if (scratch_bytes(B * H, N, d, n_kv_tiles) > kNoAllocScratch) return FATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (key_len && !aligned(key_len, 4)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!is_device_pointer(q) || !is_device_pointer(k) || !is_device_pointer(v) || !is_device_pointer(o) ||
+      !is_device_pointer(lse) || (key_len && !is_device_pointer(key_len)))
+    return FATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  NoAllocState* ns = nullptr;
+  int rc = noalloc_state(dev, &ns);
+  if (rc != FATTN_OK) return rc;
+
+  fattn::Params p;
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.key_len = key_len;
+  p.err = reinterpret_cast<int*>(ns->scratch + kNoAllocScratch);
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.n_qblocks = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
+  const long long units = (long long)B * H * p.n_qblocks;
+  if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  p.n_units = (int)units;
+  p.n_kv_tiles = n_kv_tiles;
+  p.v_mode = nullptr;
+  p.wait_limit_ns = wait_limit_ns();
+  const int grid = (int)(units < ns->num_sms ? units : ns->num_sms);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the error word must start at zero for this call; the V copy and modes are fully rewritten
+  if (cudaMemsetAsync(p.err, 0, 4 * sizeof(int), s) != cudaSuccess) return FATTN_ERR_CUDA;
+  return d == 64 ? enqueue<64>(q, k, v, p, ns->scratch, grid, s) : enqueue<128>(q, k, v, p, ns->scratch, grid, s);
+}

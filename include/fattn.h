@@ -101,6 +101,45 @@ FATTN_API const char* fattn_status_string(int status);
  */
 FATTN_API int fattn_last_error(void* stream, int* detail);
 
+/*
+ * Size of the static device scratch behind fattn_fwd_noalloc (64 MiB), plus
+ * a 256-byte error word.  Every GPU that loads the library holds this array
+ * until the process exits.
+ */
+#define FATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fattn_fwd_noalloc: fattn_fwd for callers that must not allocate device
+ * memory: code that runs where neither cudaMalloc nor a stream-ordered pool
+ * may be used, for instance inside a host framework that owns all device
+ * memory through its own arena, or a real-time path that must not take the
+ * driver's allocation locks.  The paper has no counterpart; this is a
+ * property of the library, not of the method.
+ *
+ * Arguments, layouts, semantics and results are exactly those of fattn_fwd.
+ * Instead of per-call scratch from a pool, the call uses one static device
+ * array of FATTN_NOALLOC_SCRATCH_BYTES (+256) bytes compiled into the
+ * library, and calls no cudaMalloc, cudaFree or allocating routine.
+ *
+ *   - Limit: the problem must fit the array:
+ *       round_up(B*H*N*d*2, 256) + round_up(B*H*ceil(N/128), 256) <= 64 MiB
+ *     (for example B*H <= 63 at N = 4096, d = 128); larger problems return
+ *     FATTN_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Set-up: the first call on a device (with that device current) looks up
+ *     the array's device address and sets kernel attributes; make that first
+ *     call before any stream capture.
+ *   - Sharing: every call uses the same array and it keeps the last call's
+ *     contents.  Each call clears the error word (an async memset on
+ *     `stream`) and rewrites the V copy it reads, so nothing carries over
+ *     from one call to the next; but calls whose kernels overlap on the GPU
+ *     (different streams with no ordering between them) race on the array
+ *     and give wrong results.
+ *   - Time-outs of the kernel's bounded waits land in the array's error word;
+ *     fattn_last_error() does not read it.
+ */
+FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int N, int d, float scale, int causal, const int32_t* key_len, void* stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 FATTN_API int fattn_version(void);
 

@@ -1,0 +1,76 @@
+"""fattn_fwd_noalloc: the forward for callers that may not allocate device
+memory (their framework owns all device memory, or the calling path must not
+take the driver's allocation locks).  Its scratch is a static device array
+inside the library instead of a per-call pool allocation.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test.  It passes alone in a fresh
+process and after the other tests alike.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from exact_softmax_attention_fattn_gb300 import binding
+from exact_softmax_attention_fattn_gb300.inputs import Workload, make_inputs
+from tests.gpu_helpers import bits_to_device, compare
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc():
+    lib = binding.load_library()
+    fn = lib.fattn_fwd_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int,
+                                                                ctypes.c_void_p, ctypes.c_void_p]
+    return fn
+
+
+def _check_against_fattn_fwd(w, dev, key_len=None):
+    """Two no-alloc calls in a row, each compared with fattn_fwd's result."""
+    import torch
+
+    x = make_inputs(w)
+    q, k, v = (bits_to_device(a, dev) for a in (x.q, x.k, x.v))
+    kl = None if key_len is None else torch.from_numpy(np.asarray(key_len, np.int32)).to(dev)
+    B, H, N, d = x.q.shape
+    o_ref = torch.empty_like(q)
+    lse_ref = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    binding.forward_into(q, k, v, o_ref, lse_ref, causal=w.causal, scale=w.softmax_scale, key_len=kl)
+    fn = _noalloc()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    outs = []
+    for _ in range(2):  # both calls go through the same static scratch
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+        st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                w.softmax_scale, int(w.causal), None if kl is None else kl.data_ptr(), stream)
+        assert st == binding.FATTN_OK, binding.status_string(st)
+        outs.append((o, lse))
+    torch.cuda.synchronize(dev)
+    ref = (o_ref.float().cpu().numpy().astype(np.float64), lse_ref.cpu().numpy().astype(np.float64))
+    for o, lse in outs:
+        compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), *ref,
+                what=f"no-alloc {w.name}")
+
+
+def test_noalloc_matches_fattn_fwd(cuda_device):
+    _check_against_fattn_fwd(Workload("na128", 2, 4, 1000, 128, True, 40), cuda_device)
+    # a different problem next, through the same scratch
+    _check_against_fattn_fwd(Workload("na64", 3, 2, 700, 64, False, 41, qk_sigma=2.0), cuda_device,
+                             key_len=[700, 5, 333])
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(cuda_device):
+    import torch
+
+    fn = _noalloc()
+    buf = torch.zeros(1024, dtype=torch.uint8, device=cuda_device)
+    ptr = buf.data_ptr()
+    # B*H = 64 at N = 4096, d = 128: the V copy alone fills the 64 MiB, the tile modes do not fit
+    st = fn(ptr, ptr, ptr, ptr, ptr, 64, 1, 4096, 128, 0.088, 1, None, torch.cuda.current_stream().cuda_stream)
+    assert st == binding.FATTN_ERR_UNSUPPORTED
