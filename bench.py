@@ -212,6 +212,23 @@ def reference_arm(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- ranks
+def aggregate_ranks(ms_total: float, flops_per_step: float, steps: int, world: int, device=None):
+    """Whole-job throughput over ranks: the slowest rank's time (MAX) and the
+    FLOPs of all ranks (SUM).  Returns (ms_per_step, TFLOP/s)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        f = torch.tensor([flops_per_step], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        ms_total, flops_per_step = float(t.item()), float(f.item())
+    ms_per_step = ms_total / steps
+    return ms_per_step, flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- CUDA leg
 def our_arm(args, rank: int, world: int, local_rank: int):
     import torch
@@ -270,14 +287,7 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     if st != binding.FATTN_OK:
         raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_total = float(sum(kernel_ms))
-    ms_max = ms_total
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    ms_per_step = ms_max / args.steps
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    ms_per_step, value = aggregate_ranks(float(sum(kernel_ms)), flops, args.steps, world, dev)
 
     # end to end through the public API with host buffers
     e2e = None

@@ -33,14 +33,20 @@ DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 unsigned long long g_wait_limit_ns = 0;
 
+// Limit of every bounded wait inside the kernel: 2 s unless FATTN_WAIT_LIMIT_MS
+// or (finer, taking precedence) FATTN_WAIT_LIMIT_US is set; read once.
 unsigned long long wait_limit_ns() {
   if (g_wait_limit_ns == 0) {
-    unsigned long long ms = 2000;
+    unsigned long long ns = 2000ull * 1000000ull;
     if (const char* e = std::getenv("FATTN_WAIT_LIMIT_MS")) {
       long long v = std::atoll(e);
-      if (v > 0) ms = (unsigned long long)v;
+      if (v > 0) ns = (unsigned long long)v * 1000000ull;
     }
-    g_wait_limit_ns = ms * 1000000ull;
+    if (const char* e = std::getenv("FATTN_WAIT_LIMIT_US")) {
+      long long v = std::atoll(e);
+      if (v > 0) ns = (unsigned long long)v * 1000ull;
+    }
+    g_wait_limit_ns = ns;
   }
   return g_wait_limit_ns;
 }

@@ -331,14 +331,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Drain: wait (bounded) for every copy that may still be in flight.
-        const uint32_t first = g > (uint32_t)C::STAGES ? g - C::STAGES : 0u;
-        for (uint32_t gi = first; gi < g; ++gi)
-          drain_wait(bar(C::B_KV_FULL + gi % C::STAGES), (gi / C::STAGES) & 1u, 20000000ull);
-        if (q_use0) drain_wait(bar(C::B_Q_FULL + 0), (q_use0 - 1) & 1u, 20000000ull);
-        if (q_use1) drain_wait(bar(C::B_Q_FULL + 1), (q_use1 - 1) & 1u, 20000000ull);
-      }
+      // Drain: wait (bounded) for every copy that may still be in flight -- after
+      // an abort anywhere in the CTA they may never have been consumed.  Loads
+      // older than the last STAGES were consumed before their slot was reused;
+      // in a normal run every phase below has already completed.
+      const uint32_t first = g > (uint32_t)C::STAGES ? g - C::STAGES : 0u;
+      for (uint32_t gi = first; gi < g; ++gi)
+        drain_wait(bar(C::B_KV_FULL + gi % C::STAGES), (gi / C::STAGES) & 1u, 20000000ull);
+      if (q_use0) drain_wait(bar(C::B_Q_FULL + 0), (q_use0 - 1) & 1u, 20000000ull);
+      if (q_use1) drain_wait(bar(C::B_Q_FULL + 1), (q_use1 - 1) & 1u, 20000000ull);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
@@ -390,6 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // prologue: S_t,0 for each tile with work
         ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(0)), kphase(0), C::B_KV_FULL + kslot(0), u);
+        issued_any = true;  // before any MMA, so an abort mid-prologue still drains
         auto prologue = [&](auto tc) {
           constexpr int t = decltype(tc)::value;
           if (!ok || w.n(t) == 0) return;
@@ -405,7 +407,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prologue(TileC<1>{});
         if (!ok) break;
         mma_commit(bar(C::B_KV_EMPTY + kslot(0)));
-        issued_any = true;
 
         const uint8_t* modes = p.v_mode + (size_t)w.bh * p.n_kv_tiles;
         int vmode_next = __ldg(modes);

@@ -1,0 +1,52 @@
+"""Failure detection without a GPU fault.
+
+Every wait inside the kernel is bounded.  A child process sets the bound to
+1 microsecond, far below the latency of the first tile load, so the waits run
+out for real; the kernel must record the time-out (status, role, barrier,
+work unit), drain its own copies and MMAs, free tensor memory and return, and
+the host must read FATTN_ERR_TIMEOUT from fattn_last_error.  The child then
+runs ordinary CUDA work to show the context is still usable.
+"""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import json, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+from exact_softmax_attention_fattn_gb300 import binding
+from exact_softmax_attention_fattn_gb300.inputs import Workload, make_inputs
+x = make_inputs(Workload("to", 1, 4, 2048, 128, True, 50))
+dev = torch.device("cuda:0")
+q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in (x.q, x.k, x.v))
+o = torch.empty_like(q); lse = torch.empty((1, 4, 2048), dtype=torch.float32, device=dev)
+binding.forward_into(q, k, v, o, lse, causal=True)
+st, detail = binding.last_error()
+again, _ = binding.last_error()          # the flag is cleared once read
+a = torch.randn(512, 512, device=dev)
+ok = bool(torch.isfinite(a @ a).all().item())
+torch.cuda.synchronize()
+print(json.dumps({"status": st, "detail": detail, "again": again, "context_ok": ok}))
+"""
+
+
+def test_bounded_wait_times_out_and_reports(cuda_device):
+    env = dict(os.environ, FATTN_WAIT_LIMIT_US="1")
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == 4  # FATTN_ERR_TIMEOUT
+    status, role, barrier, unit = res["detail"]
+    assert status == 4 and role in (1, 2, 3) and barrier >= 0 and unit >= 0
+    assert res["again"] == 0
+    assert res["context_ok"]
