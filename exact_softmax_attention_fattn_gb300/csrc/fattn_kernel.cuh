@@ -220,6 +220,7 @@ __device__ __forceinline__ bool wait_slow(const Waiter& w, uint32_t bar, uint32_
 }
 
 __device__ __forceinline__ bool wait_bar(const Waiter& w, uint32_t bar, uint32_t parity, int bar_id, int unit) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(w, bar, parity, bar_id, unit);
 }
@@ -308,13 +309,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_3d(dst + pn * PANEL_BYTES, &tmap_q, bar(C::B_Q_FULL + t), 64 * pn, w.r0 + t * BM, w.bh);
         ++q_use;
       };
+      // L2 prefetch: K/V tiles PF steps ahead of the ring, and the next unit's
+      // Q tiles and first K/V tiles, so the ring's TMA loads hit L2.
+      constexpr int PF = 3;
+      auto prefetch_kv = [&](const Unit& w, int j) {
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+          tma_prefetch_l2_3d(&tmap_k, 64 * pn, j * BN, w.bh);
+          tma_prefetch_l2_3d(&tmap_v, 64 * pn, j * BN, w.bh);
+        }
+      };
       for (int r = 0; ok && r * G < p.n_units; ++r) {
         const int u = unit_of(r, cta, G);
         if (u >= p.n_units) continue;
         const Unit w = decode_unit(p, u);
+        if (r == 0 || unit_of(r - 1, cta, G) >= p.n_units)
+          for (int j = 1; j < PF && j < w.nkv; ++j) prefetch_kv(w, j);
+        {
+          // the next unit this CTA will process
+          int rn = r + 1;
+          while (rn * G < p.n_units && unit_of(rn, cta, G) >= p.n_units) ++rn;
+          if (rn * G < p.n_units) {
+            const Unit wn = decode_unit(p, unit_of(rn, cta, G));
+#pragma unroll
+            for (int t = 0; t < QT; ++t)
+              if (wn.n(t) > 0)
+#pragma unroll
+                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(&tmap_q, 64 * pn, wn.r0 + t * BM, wn.bh);
+            for (int j = 0; j < PF && j < wn.nkv; ++j) prefetch_kv(wn, j);
+          }
+        }
         load_q(TileC<0>{}, w, u, q_use0);
         load_q(TileC<1>{}, w, u, q_use1);
         for (int j = 0; ok && j < w.nkv; ++j) {
+          if (j + PF < w.nkv) prefetch_kv(w, j + PF);
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
             const uint32_t slot = g % C::STAGES;
@@ -343,7 +371,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop so that descriptors and addresses are
+    // warp-uniform; elect.sync inside each MMA / commit picks the one lane
+    // that issues it.  Every wait result is made warp-uniform.
+    {
       waiter.role = ROLE_MMA;
       constexpr uint32_t IDESC_S = idesc_f16kind(BM, BN, true, false);      // Q, K bf16
       constexpr uint32_t IDESC_PV_F16 = idesc_f16kind(BM, D, false, true);  // P, V f16; V MN-major
@@ -355,27 +386,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       bool issued_any = false;
 
+      // Descriptors: built once per operand tile, then advanced along K by adding
+      // the byte offset >> 4 to the start-address field (no carry: smem < 256 KB).
+      const uint64_t q_desc0 = smem_desc(base + C::Q_OFF, 16, 1024);
+      const uint64_t ring_kdesc0 = smem_desc(base + C::RING_OFF, 16, 1024);
+      const uint64_t ring_vdesc0 = smem_desc(base + C::RING_OFF, PANEL_BYTES, 1024);
+
       // S_t = Q_t K^T from the K tile in `slot`.
       auto issue_s = [&](auto tc, uint32_t slot) {
         constexpr int t = decltype(tc)::value;
-        const uint32_t qa = base + C::Q_OFF + (uint32_t)t * C::TILE_BYTES;
-        const uint32_t ka = base + C::RING_OFF + slot * C::TILE_BYTES;
+        const uint64_t qd = q_desc0 + (uint64_t)((t * C::TILE_BYTES) >> 4);
+        const uint64_t kd = ring_kdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk / 4) * PANEL_BYTES + (uint32_t)(kk % 4) * 32u;
-          mma_ss(tmem + TMEM_S0 + 128u * t, smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk / 4) * PANEL_BYTES + (kk % 4) * 32u) >> 4);
+          mma_ss_w(tmem + TMEM_S0 + 128u * t, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_t V with P in tensor memory, V (keys x D, D contiguous) in `slot`.
-      auto issue_pv = [&](auto tc, uint32_t slot, bool accumulate, uint32_t idesc_pv) {
+      auto issue_pv = [&](auto tc, uint32_t slot, uint32_t accumulate, uint32_t idesc_pv) {
         constexpr int t = decltype(tc)::value;
-        const uint32_t va = base + C::RING_OFF + slot * C::TILE_BYTES;
+        const uint64_t vd = ring_vdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts(tmem + TMEM_O0 + 128u * t, tmem + TMEM_S0 + 128u * t + 8u * kk,
-                 smem_desc(va + (uint32_t)kk * 2048u, PANEL_BYTES, 1024), idesc_pv,
-                 (accumulate || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + TMEM_O0 + 128u * t, tmem + TMEM_S0 + 128u * t + 8u * kk, vd + (uint64_t)((kk * 2048u) >> 4),
+                 idesc_pv, kk > 0 ? 1u : accumulate);
         }
       };
 
@@ -391,57 +426,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // prologue: S_t,0 for each tile with work
         ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(0)), kphase(0), C::B_KV_FULL + kslot(0), u);
+          ok = __all_sync(0xffffffffu, ok);
         issued_any = true;  // before any MMA, so an abort mid-prologue still drains
         auto prologue = [&](auto tc) {
           constexpr int t = decltype(tc)::value;
           if (!ok || w.n(t) == 0) return;
           ok = wait_bar(waiter, bar(C::B_Q_FULL + t), q_use[t] & 1u, C::B_Q_FULL + t, u);
+          ok = __all_sync(0xffffffffu, ok);
           if (!ok) return;
           ++q_use[t];
           tc_fence_after();
           issue_s(tc, kslot(0));
-          mma_commit(bar(C::B_S_FULL + t));
-          if (w.n(t) == 1) mma_commit(bar(C::B_Q_EMPTY + t));
+          mma_commit_w(bar(C::B_S_FULL + t));
+          if (w.n(t) == 1) mma_commit_w(bar(C::B_Q_EMPTY + t));
         };
         prologue(TileC<0>{});
         prologue(TileC<1>{});
         if (!ok) break;
-        mma_commit(bar(C::B_KV_EMPTY + kslot(0)));
+        mma_commit_w(bar(C::B_KV_EMPTY + kslot(0)));
 
         const uint8_t* modes = p.v_mode + (size_t)w.bh * p.n_kv_tiles;
         int vmode_next = __ldg(modes);
         for (int j = 0; ok && j < w.nkv; ++j) {
           const uint32_t idesc_pv = vmode_next == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
           if (j + 1 < w.nkv) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+          // V_j and K_j+1 are almost always resident already: check both before
+          // waiting on P, so that P's arrival is followed by back-to-back MMAs.
           ok = wait_bar(waiter, bar(C::B_KV_FULL + vslot(j)), vphase(j), C::B_KV_FULL + vslot(j), u);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok && j + 1 < w.nkv)
+            ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(j + 1)), kphase(j + 1), C::B_KV_FULL + kslot(j + 1), u);
+          ok = __all_sync(0xffffffffu, ok);
           // O_t += P_t V_j, then S_t,j+1 = Q_t K_j+1^T (tile 1's MMAs run while tile 0's softmax works)
           auto step = [&](auto tc) {
             constexpr int t = decltype(tc)::value;
             if (!ok || j >= w.n(t)) return;
             if (j == 0) {
               ok = wait_bar(waiter, bar(C::B_O_EMPTY + t), (units_done[t] & 1u) ^ 1u, C::B_O_EMPTY + t, u);
+          ok = __all_sync(0xffffffffu, ok);
               if (!ok) return;
             }
             ok = wait_bar(waiter, bar(C::B_P_FULL + t), pv_cnt[t] & 1u, C::B_P_FULL + t, u);
+          ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             ++pv_cnt[t];
             tc_fence_after();
-            issue_pv(tc, vslot(j), j > 0, idesc_pv);
-            if (j == w.n(t) - 1) mma_commit(bar(C::B_O_FULL + t));
+            issue_pv(tc, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
+            if (j == w.n(t) - 1) mma_commit_w(bar(C::B_O_FULL + t));
             if (j + 1 < w.n(t)) {
-              ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(j + 1)), kphase(j + 1), C::B_KV_FULL + kslot(j + 1), u);
-              if (!ok) return;
-              tc_fence_after();
               issue_s(tc, kslot(j + 1));
-              mma_commit(bar(C::B_S_FULL + t));
-              if (j + 1 == w.n(t) - 1) mma_commit(bar(C::B_Q_EMPTY + t));
+              mma_commit_w(bar(C::B_S_FULL + t));
+              if (j + 1 == w.n(t) - 1) mma_commit_w(bar(C::B_Q_EMPTY + t));
             }
           };
           step(TileC<0>{});
           step(TileC<1>{});
           if (!ok) break;
-          mma_commit(bar(C::B_KV_EMPTY + vslot(j)));
-          if (j + 1 < w.nkv) mma_commit(bar(C::B_KV_EMPTY + kslot(j + 1)));
+          mma_commit_w(bar(C::B_KV_EMPTY + vslot(j)));
+          if (j + 1 < w.nkv) mma_commit_w(bar(C::B_KV_EMPTY + kslot(j + 1)));
         }
         g += 2u * (uint32_t)w.nkv;
         if (w.n0 > 0) ++units_done[0];
@@ -449,7 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // Drain: every MMA this thread issued has completed before TMEM is freed.
       if (issued_any) {
-        mma_commit(bar(C::B_DRAIN));
+        mma_commit_w(bar(C::B_DRAIN));
         drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
       }
     }
