@@ -101,9 +101,10 @@ struct Cfg {
   static constexpr int B_O_FULL = 8;                     // [2]
   static constexpr int B_O_EMPTY = 10;                   // [2]
   static constexpr int B_DRAIN = 12;                     // [1]
-  static constexpr int B_KV_FULL = 13;                   // [STAGES]
-  static constexpr int B_KV_EMPTY = 13 + STAGES;         // [STAGES]
-  static constexpr int NUM_BARS = 13 + 2 * STAGES;
+  static constexpr int B_PH_FULL = 13;                   // [2] first half of P (keys 0-63) written
+  static constexpr int B_KV_FULL = 15;                   // [STAGES]
+  static constexpr int B_KV_EMPTY = 15 + STAGES;         // [STAGES]
+  static constexpr int NUM_BARS = 15 + 2 * STAGES;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
   static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -235,6 +236,41 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 template <int T>
 using TileC = std::integral_constant<int, T>;
 
+// 2^x for a pair on the FMA pipe, to take part of the exponentials off the
+// MUFU unit.  Cody-Waite style split x = n + f with n = round(x) (the
+// 1.5*2^23 rounding trick) and f in [-1/2, 1/2]; 2^f by a cubic with
+// coefficients fitted here by Remez exchange for minimum relative error on
+// [-1/2, 1/2] (max relative error 7.5e-5 in fp32, below the fp16 rounding of
+// P); 2^n is added into the exponent field.  x is clamped at -126 so the
+// exponent never wraps (2^-126 is zero for every later use).
+constexpr float EXP2_C0 = 0.9999280571937561f;
+constexpr float EXP2_C1 = 0.6932609677314758f;
+constexpr float EXP2_C2 = 0.2426111251115799f;
+constexpr float EXP2_C3 = 0.0551716685295105f;
+constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23
+
+__device__ __forceinline__ void exp2_poly_pair(float x0, float x1, float& y0, float& y1) {
+  x0 = fmaxf(x0, -126.0f);
+  x1 = fmaxf(x1, -126.0f);
+  const uint64_t x = f2_pack(x0, x1);
+  const uint64_t t = f2_add(x, f2_pack(ROUND_MAGIC, ROUND_MAGIC));      // n in the low mantissa bits
+  const uint64_t r = f2_add(t, f2_pack(-ROUND_MAGIC, -ROUND_MAGIC));    // n as a float
+  const uint64_t f = f2_fma(r, f2_pack(-1.0f, -1.0f), x);               // x - n
+  uint64_t q = f2_fma(f2_pack(EXP2_C3, EXP2_C3), f, f2_pack(EXP2_C2, EXP2_C2));
+  q = f2_fma(q, f, f2_pack(EXP2_C1, EXP2_C1));
+  q = f2_fma(q, f, f2_pack(EXP2_C0, EXP2_C0));
+  float t0, t1, q0, q1;
+  f2_unpack(t, t0, t1);
+  f2_unpack(q, q0, q1);
+  y0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+  y1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+}
+
+// Pairs (of 32 per half row) whose exponentials are emulated: 3 of every 8.
+__host__ __device__ constexpr bool exp2_emulated(int pair) {
+  return (pair & 7) == 1 || (pair & 7) == 4 || (pair & 7) == 6;
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -263,6 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(C::B_P_FULL + t), BM);
       mbar_init(bar(C::B_O_FULL + t), 1);
       mbar_init(bar(C::B_O_EMPTY + t), BM);
+      mbar_init(bar(C::B_PH_FULL + t), BM);
     }
     mbar_init(bar(C::B_DRAIN), 1);
     for (int s = 0; s < C::STAGES; ++s) {
@@ -403,12 +440,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mma_ss_w(tmem + TMEM_S0 + 128u * t, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t (+)= P_t V with P in tensor memory, V (keys x D, D contiguous) in `slot`.
-      auto issue_pv = [&](auto tc, uint32_t slot, uint32_t accumulate, uint32_t idesc_pv) {
+      // P in tensor memory, V (keys x D, D contiguous) in `slot`.
+      // O_t (+)= P_t V over keys [16*KB, 16*KE) of the tile.
+      auto issue_pv = [&](auto tc, auto kb, auto ke, uint32_t slot, uint32_t accumulate, uint32_t idesc_pv) {
         constexpr int t = decltype(tc)::value;
+        constexpr int KB = decltype(kb)::value, KE = decltype(ke)::value;
         const uint64_t vd = ring_vdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
+        for (int kk = KB; kk < KE; ++kk) {
           mma_ts_w(tmem + TMEM_O0 + 128u * t, tmem + TMEM_S0 + 128u * t + 8u * kk, vd + (uint64_t)((kk * 2048u) >> 4),
                  idesc_pv, kk > 0 ? 1u : accumulate);
         }
@@ -466,12 +505,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = __all_sync(0xffffffffu, ok);
               if (!ok) return;
             }
+            // first half of P (keys 0-63), then the rest
+            ok = wait_bar(waiter, bar(C::B_PH_FULL + t), pv_cnt[t] & 1u, C::B_PH_FULL + t, u);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) return;
+            tc_fence_after();
+            issue_pv(tc, TileC<0>{}, TileC<BN / 32>{}, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
             ok = wait_bar(waiter, bar(C::B_P_FULL + t), pv_cnt[t] & 1u, C::B_P_FULL + t, u);
-          ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             ++pv_cnt[t];
             tc_fence_after();
-            issue_pv(tc, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
+            issue_pv(tc, TileC<BN / 32>{}, TileC<BN / 16>{}, vslot(j), 1u, idesc_pv);
             if (j == w.n(t) - 1) mma_commit_w(bar(C::B_O_FULL + t));
             if (j + 1 < w.n(t)) {
               issue_s(tc, kslot(j + 1));
@@ -508,6 +553,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t o_addr = tmem + lane_off + TMEM_O0 + 128u * t;
     const uint32_t bar_s_full = bar(C::B_S_FULL + t);
     const uint32_t bar_p_full = bar(C::B_P_FULL + t);
+    const uint32_t bar_ph_full = bar(C::B_PH_FULL + t);
     const uint32_t bar_o_full = bar(C::B_O_FULL + t);
     const uint32_t bar_o_empty = bar(C::B_O_EMPTY + t);
     const float c = p.scale_log2;
@@ -549,7 +595,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++s_cnt;
         tc_fence_after();
 
-        float s[BN];
+        float s[BN];  // this row of S, for the row max only
         {
           uint32_t r32[BN];
           tmem_ld128(s_addr, r32);
@@ -585,35 +631,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const float mc = (m_ref == -INFINITY) ? 0.0f : m_ref * c;
 
-        // p = 2^(s*c - m*c): kept in fp32 for l, rounded once for PV, to fp16
-        // when this V tile is stored in fp16 (the usual case: 11 significant
-        // bits) and to bf16 when it is not.  Masked entries are exactly zero.
-        float sum8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
-        uint32_t pk[BN / 2];
-        auto exp_pack = [&](auto pack) {
-#pragma unroll
-          for (int i = 0; i < BN; i += 2) {
-            float p0 = ex2(fmaf(s[i], c, -mc));
-            float p1 = ex2(fmaf(s[i + 1], c, -mc));
-            if (masked_tile) {
-              p0 = i < vis_n ? p0 : 0.0f;
-              p1 = i + 1 < vis_n ? p1 : 0.0f;
-            }
-            pk[i / 2] = pack(p0, p1);
-            sum8[(i / 2) % 8] += p0 + p1;
-          }
-        };
-        if (vmode == VMODE_F16)
-          exp_pack([](float a, float b) { return pack_f16x2(a, b); });
-        else
-          exp_pack([](float a, float b) { return pack_bf16x2(a, b); });
-        const float rs = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        l = l * alpha + rs;
-
-        // correction: rescale this row of O (PV of the previous tile has completed,
-        // since S of this tile was issued after it and has completed)
+        // correction first: rescale this row of O (PV of the previous tile has
+        // completed, since S of this tile was issued after it and has completed)
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -625,18 +644,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_st32(o_addr + 32u * cc, r32);
           }
         }
-        // P over the first 64 columns of S
-        {
-          uint32_t r32[32];
+
+        // p = 2^(s*c - m*c): kept in fp32 for l, rounded once for PV, to fp16
+        // when this V tile is stored in fp16 (the usual case: 11 significant
+        // bits) and to bf16 when it is not.  Masked entries are exactly zero.
+        // Each half row (64 keys) is stored and released on its own so that
+        // the P V product can start on the first half.
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nmc2 = f2_pack(-mc, -mc);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        auto half_row = [&](int h, auto pack) {
+          // S of this half row again (cheap to reload; keeps registers free)
+          uint32_t sh[64];
+          tmem_ld64(s_addr + 64u * h, sh);
+          tmem_ld_wait(sh);
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r32[i] = pk[i];
-          tmem_st32(s_addr, r32);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r32[i] = pk[32 + i];
-          tmem_st32(s_addr + 32u, r32);
-        }
-        tmem_st_wait();
-        tc_fence_before();
+          for (int q = 0; q < 32; ++q) {
+            const int i = 64 * h + 2 * q;
+            float x0, x1, p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[2 * q]), __uint_as_float(sh[2 * q + 1])), c2, nmc2), x0, x1);
+            if (exp2_emulated(q)) {
+              exp2_poly_pair(x0, x1, p0, p1);
+            } else {
+              p0 = ex2(x0);
+              p1 = ex2(x1);
+            }
+            if (masked_tile) {
+              p0 = i < vis_n ? p0 : 0.0f;
+              p1 = i + 1 < vis_n ? p1 : 0.0f;
+            }
+            acc[q % 4] = f2_add(acc[q % 4], f2_pack(p0, p1));
+            pk[q] = pack(p0, p1);
+          }
+          tmem_st32(s_addr + 32u * h, pk);
+          tmem_st_wait();
+          tc_fence_before();
+        };
+        auto both_halves = [&](auto pack) {
+          half_row(0, pack);
+          mbar_arrive(bar_ph_full);
+          half_row(1, pack);
+        };
+        if (vmode == VMODE_F16)
+          both_halves([](float a, float b) { return pack_f16x2(a, b); });
+        else
+          both_halves([](float a, float b) { return pack_bf16x2(a, b); });
+        float a0, a1, a2, a3, a4, a5, a6, a7;
+        f2_unpack(acc[0], a0, a1);
+        f2_unpack(acc[1], a2, a3);
+        f2_unpack(acc[2], a4, a5);
+        f2_unpack(acc[3], a6, a7);
+        const float rs = ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+        l = l * alpha + rs;
         mbar_arrive(bar_p_full);
       }
       if (!ok) break;
