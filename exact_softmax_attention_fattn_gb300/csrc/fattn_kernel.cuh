@@ -201,11 +201,14 @@ struct Waiter {
   int role;
 };
 
-// Returns false (and raises the CTA's abort flag) if the wait gave up.
+// Returns false (and raises the CTA's abort flag) if the wait gave up.  The
+// thread is suspended in hardware between checks (try_wait with a time hint),
+// so waiting warps take no issue slots from the warps that compute.
 __device__ __forceinline__ bool wait_slow(const Waiter& w, uint32_t bar, uint32_t parity, int bar_id, int unit) {
   const uint64_t t0 = globaltimer_ns();
+  const uint32_t hint = w.limit_ns < 1000000ull ? (uint32_t)w.limit_ns : 1000000u;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
     if (*w.abort_flag) return false;
     if (globaltimer_ns() - t0 > w.limit_ns) {
       *w.abort_flag = 1;
@@ -222,7 +225,6 @@ __device__ __forceinline__ bool wait_slow(const Waiter& w, uint32_t bar, uint32_
 
 __device__ __forceinline__ bool wait_bar(const Waiter& w, uint32_t bar, uint32_t parity, int bar_id, int unit) {
   if (mbar_test_wait(bar, parity)) return true;
-  if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(w, bar, parity, bar_id, unit);
 }
 
@@ -236,40 +238,6 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 template <int T>
 using TileC = std::integral_constant<int, T>;
 
-// 2^x for a pair on the FMA pipe, to take part of the exponentials off the
-// MUFU unit.  Cody-Waite style split x = n + f with n = round(x) (the
-// 1.5*2^23 rounding trick) and f in [-1/2, 1/2]; 2^f by a cubic with
-// coefficients fitted here by Remez exchange for minimum relative error on
-// [-1/2, 1/2] (max relative error 7.5e-5 in fp32, below the fp16 rounding of
-// P); 2^n is added into the exponent field.  x is clamped at -126 so the
-// exponent never wraps (2^-126 is zero for every later use).
-constexpr float EXP2_C0 = 0.9999280571937561f;
-constexpr float EXP2_C1 = 0.6932609677314758f;
-constexpr float EXP2_C2 = 0.2426111251115799f;
-constexpr float EXP2_C3 = 0.0551716685295105f;
-constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23
-
-__device__ __forceinline__ void exp2_poly_pair(float x0, float x1, float& y0, float& y1) {
-  x0 = fmaxf(x0, -126.0f);
-  x1 = fmaxf(x1, -126.0f);
-  const uint64_t x = f2_pack(x0, x1);
-  const uint64_t t = f2_add(x, f2_pack(ROUND_MAGIC, ROUND_MAGIC));      // n in the low mantissa bits
-  const uint64_t r = f2_add(t, f2_pack(-ROUND_MAGIC, -ROUND_MAGIC));    // n as a float
-  const uint64_t f = f2_fma(r, f2_pack(-1.0f, -1.0f), x);               // x - n
-  uint64_t q = f2_fma(f2_pack(EXP2_C3, EXP2_C3), f, f2_pack(EXP2_C2, EXP2_C2));
-  q = f2_fma(q, f, f2_pack(EXP2_C1, EXP2_C1));
-  q = f2_fma(q, f, f2_pack(EXP2_C0, EXP2_C0));
-  float t0, t1, q0, q1;
-  f2_unpack(t, t0, t1);
-  f2_unpack(q, q0, q1);
-  y0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-  y1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
-}
-
-// Pairs (of 32 per half row) whose exponentials are emulated: 3 of every 8.
-__host__ __device__ constexpr bool exp2_emulated(int pair) {
-  return (pair & 7) == 1 || (pair & 7) == 4 || (pair & 7) == 6;
-}
 
 // ------------------------------------------------------------------ the kernel
 template <int D>
@@ -664,12 +632,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int i = 64 * h + 2 * q;
             float x0, x1, p0, p1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[2 * q]), __uint_as_float(sh[2 * q + 1])), c2, nmc2), x0, x1);
-            if (exp2_emulated(q)) {
-              exp2_poly_pair(x0, x1, p0, p1);
-            } else {
-              p0 = ex2(x0);
-              p1 = ex2(x1);
-            }
+            p0 = ex2(x0);
+            p1 = ex2(x1);
             if (masked_tile) {
               p0 = i < vis_n ? p0 : 0.0f;
               p1 = i + 1 < vis_n ? p1 : 0.0f;
