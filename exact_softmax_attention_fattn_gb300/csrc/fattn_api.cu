@@ -134,9 +134,11 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Scratch of one call: V in its per-tile storage type, then one mode byte per tile.
+// Scratch of one call: V in its per-tile storage type, then one mode byte per
+// tile, each head's row of modes padded to a multiple of 8 bytes.
 size_t scratch_bytes(int BH, int N, int D, int n_tiles) {
-  return round_up((size_t)BH * (size_t)N * (size_t)D * 2u, 256) + round_up((size_t)BH * (size_t)n_tiles, 256);
+  return round_up((size_t)BH * (size_t)N * (size_t)D * 2u, 256) +
+         round_up((size_t)BH * round_up((size_t)n_tiles, 8), 256);
 }
 
 // Enqueues the V pre-pass and the attention kernel; `scratch` must hold scratch_bytes().
@@ -154,7 +156,7 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
     return FATTN_ERR_CUDA;
   const long long prepass_blocks = (long long)BH * p.n_kv_tiles;
   fattn::fattn_v_prepass_kernel<D><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
-      reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.n_kv_tiles);
+      reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.n_kv_tiles, p.mode_stride);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   fattn::fattn_fwd_kernel<D><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
@@ -215,7 +217,8 @@ extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, 
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
   p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
-  if ((long long)B * H * p.n_kv_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  p.mode_stride = (p.n_kv_tiles + 7) / 8 * 8;
+  if ((long long)B * H * p.mode_stride > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.v_mode = nullptr;
   p.wait_limit_ns = wait_limit_ns();
   const int grid = (int)(units < ds->num_sms ? units : ds->num_sms);
@@ -324,7 +327,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   const int n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
-  if ((long long)B * H * n_kv_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * ((n_kv_tiles + 7) / 8 * 8) > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   // the static scratch bounds the problem size
   if (scratch_bytes(B * H, N, d, n_kv_tiles) > kNoAllocScratch) return FATTN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
@@ -356,6 +359,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
   p.n_kv_tiles = n_kv_tiles;
+  p.mode_stride = (n_kv_tiles + 7) / 8 * 8;
   p.v_mode = nullptr;
   p.wait_limit_ns = wait_limit_ns();
   const int grid = (int)(units < ns->num_sms ? units : ns->num_sms);

@@ -49,10 +49,10 @@ constexpr int NUM_THREADS = 384;
 // Register split (setmaxnreg): the block launches with LAUNCH_REGS per thread
 // (ptxas' cap for 384 threads, one SM); the two softmax warpgroups grow to
 // SOFTMAX_REGS and the producer/MMA warpgroup shrinks to OTHER_REGS.  The
-// split uses exactly the launch allocation: 256*200 + 128*104 = 384*168.
+// split uses exactly the launch allocation: 256*192 + 128*120 = 384*168.
 constexpr int LAUNCH_REGS = 168;
-constexpr int SOFTMAX_REGS = 200;
-constexpr int OTHER_REGS = 104;
+constexpr int SOFTMAX_REGS = 192;
+constexpr int OTHER_REGS = 120;
 static_assert(256 * SOFTMAX_REGS + 128 * OTHER_REGS <= NUM_THREADS * LAUNCH_REGS, "register split exceeds launch");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S0 = 0;    // S_t at column 128*t, P_t packed into its first 64 columns
@@ -72,7 +72,7 @@ struct Params {
   __nv_bfloat16* o;
   float* lse;
   const int32_t* key_len;  // [B] or nullptr
-  const uint8_t* v_mode;   // [B*H, n_kv_tiles]: storage type of each V tile (VMODE_*)
+  const uint8_t* v_mode;   // [B*H, mode_stride]: storage type of each V tile (VMODE_*)
   int* err;                // int[4]
   int B, H, N;
   float scale;       // softmax scale (natural units), >= 0
@@ -81,6 +81,7 @@ struct Params {
   int n_qblocks;  // ceil(N / 256)
   int n_units;    // B * H * n_qblocks
   int n_kv_tiles; // ceil(N / 128)
+  int mode_stride; // n_kv_tiles rounded up to 8: modes are read 8 at a time
   unsigned long long wait_limit_ns;
 };
 
@@ -149,7 +150,7 @@ struct Unit {
   __device__ __forceinline__ bool valid(int t) const { return t ? valid1 : valid0; }
 };
 
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int kl_raw) {
   Unit w;
   const int BH = p.B * p.H;
   const int round = u / BH;
@@ -157,11 +158,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   w.b = w.bh / p.H;
   const int qb = p.n_qblocks - 1 - round;  // latest (heaviest under causal) blocks first
   w.r0 = qb * (QT * BM);
-  int kl = p.N;
-  if (p.key_len) {
-    kl = __ldg(p.key_len + w.b);
-    kl = kl < 0 ? 0 : (kl > p.N ? p.N : kl);
-  }
+  const int kl = kl_raw < 0 ? 0 : (kl_raw > p.N ? p.N : kl_raw);
   w.kl = kl;
   int nn[QT], ml[QT];
   bool vv[QT];
@@ -192,6 +189,64 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
 // r*G + G-1-c (r odd).  Units are ordered heaviest first, so the snake pairs
 // heavy and light units on each CTA.
 __device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
+
+// The units of one CTA in schedule order, read one unit ahead: the next
+// unit's key length and first V-tile storage mode are requested once
+// the current unit is under way (at its second tile), so no role waits on a
+// global load at a unit boundary, where the epilogue's output stores occupy
+// the memory pipeline.
+struct UnitIter {
+  int r, u, kl_raw;        // current unit (u < 0: done)
+  int mode0;               // storage mode of its first V tile
+  int r_next, u_next;      // the one after it
+  int kl_next, mode_next;
+  int next_bh;             // its batch*head, for the loads below
+  int fetch_at;            // tile index at which the loads are issued (runtime value)
+
+  __device__ __forceinline__ static int round_from(const Params& p, int r, int cta, int G) {
+    while (r * G < p.n_units && unit_of(r, cta, G) >= p.n_units) ++r;
+    return r * G < p.n_units ? r : -1;
+  }
+  // the two loads for the next unit; cheap enough to sit inside the tile loop
+  __device__ __forceinline__ void load_next(const Params& p) {
+    if (u_next < 0) return;
+    kl_next = p.key_len ? __ldg(p.key_len + next_bh / p.H) : p.N;
+    mode_next = __ldg(p.v_mode + (size_t)next_bh * p.mode_stride);
+  }
+  __device__ __forceinline__ void locate_next(const Params& p, int cta, int G) {
+    r_next = r < 0 ? -1 : round_from(p, r + 1, cta, G);
+    u_next = r_next < 0 ? -1 : unit_of(r_next, cta, G);
+    next_bh = u_next < 0 ? 0 : u_next % (p.B * p.H);
+    fetch_at = 1;
+  }
+  __device__ __forceinline__ void begin(const Params& p, int cta, int G) {
+    r = round_from(p, 0, cta, G);
+    u = r < 0 ? -1 : unit_of(r, cta, G);
+    if (u >= 0) {
+      const int bh = u % (p.B * p.H);
+      kl_raw = p.key_len ? __ldg(p.key_len + bh / p.H) : p.N;
+      mode0 = __ldg(p.v_mode + (size_t)bh * p.mode_stride);
+    }
+    locate_next(p, cta, G);
+    load_next(p);
+    fetch_at = -1;  // already requested
+  }
+  // call once per tile with its index; issues the next unit's loads at tile `fetch_at`
+  __device__ __forceinline__ void at_tile(const Params& p, int j) {
+    if (j == fetch_at) {
+      load_next(p);
+      fetch_at = -1;
+    }
+  }
+  __device__ __forceinline__ void advance(const Params& p, int cta, int G) {
+    if (fetch_at >= 0) load_next(p);  // the unit ended before its request point
+    r = r_next;
+    u = u_next;
+    kl_raw = kl_next;
+    mode0 = mode_next;
+    locate_next(p, cta, G);
+  }
+};
 
 // ------------------------------------------------------------------ bounded wait
 struct Waiter {
@@ -237,6 +292,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsign
 
 template <int T>
 using TileC = std::integral_constant<int, T>;
+
+// f(integral_constant<int, I>) for I = 0 .. N-1, unrolled at compile time.
+template <int N, int I = 0, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for<N, I + 1>(f);
+  }
+}
 
 
 // ------------------------------------------------------------------ the kernel
@@ -324,18 +388,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_prefetch_l2_3d(&tmap_v, 64 * pn, j * BN, w.bh);
         }
       };
-      for (int r = 0; ok && r * G < p.n_units; ++r) {
-        const int u = unit_of(r, cta, G);
-        if (u >= p.n_units) continue;
-        const Unit w = decode_unit(p, u);
-        if (r == 0 || unit_of(r - 1, cta, G) >= p.n_units)
+      UnitIter it;
+      it.begin(p, cta, G);
+      bool first_unit = true;
+      for (; ok && it.u >= 0; it.advance(p, cta, G)) {
+        const int u = it.u;
+        const Unit w = decode_unit(p, u, it.kl_raw);
+        it.at_tile(p, it.fetch_at);
+        if (first_unit)
           for (int j = 1; j < PF && j < w.nkv; ++j) prefetch_kv(w, j);
+        first_unit = false;
         {
           // the next unit this CTA will process
-          int rn = r + 1;
-          while (rn * G < p.n_units && unit_of(rn, cta, G) >= p.n_units) ++rn;
-          if (rn * G < p.n_units) {
-            const Unit wn = decode_unit(p, unit_of(rn, cta, G));
+          if (it.u_next >= 0) {
+            const Unit wn = decode_unit(p, it.u_next, it.kl_next);
 #pragma unroll
             for (int t = 0; t < QT; ++t)
               if (wn.n(t) > 0)
@@ -402,11 +468,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int t = decltype(tc)::value;
         const uint64_t qd = q_desc0 + (uint64_t)((t * C::TILE_BYTES) >> 4);
         const uint64_t kd = ring_kdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk / 4) * PANEL_BYTES + (kk % 4) * 32u) >> 4);
-          mma_ss_w(tmem + TMEM_S0 + 128u * t, qd + off, kd + off, IDESC_S, kk > 0 ? 1u : 0u);
-        }
+        const uint32_t dt = tmem + TMEM_S0 + 128u * t;
+        static_for<D / 16>([&](auto kc) {
+          constexpr int kk = decltype(kc)::value;
+          constexpr uint32_t off = ((kk / 4) * PANEL_BYTES + (kk % 4) * 32u) >> 4;
+          mma_ss_w_off<off>(dt, qd, kd, IDESC_S, kk > 0 ? 1u : 0u);
+        });
       };
       // P in tensor memory, V (keys x D, D contiguous) in `slot`.
       // O_t (+)= P_t V over keys [16*KB, 16*KE) of the tile.
@@ -414,18 +481,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int t = decltype(tc)::value;
         constexpr int KB = decltype(kb)::value, KE = decltype(ke)::value;
         const uint64_t vd = ring_vdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-#pragma unroll
-        for (int kk = KB; kk < KE; ++kk) {
-          mma_ts_w(tmem + TMEM_O0 + 128u * t, tmem + TMEM_S0 + 128u * t + 8u * kk, vd + (uint64_t)((kk * 2048u) >> 4),
-                 idesc_pv, kk > 0 ? 1u : accumulate);
-        }
+        const uint32_t dt = tmem + TMEM_O0 + 128u * t;
+        const uint32_t at = tmem + TMEM_S0 + 128u * t;
+        static_for<KE - KB>([&](auto kc) {
+          constexpr int kk = KB + decltype(kc)::value;
+          constexpr uint32_t boff = (kk * 2048u) >> 4;  // 16 keys = two 1024-byte row groups
+          constexpr uint32_t acol = 8u * kk;            // 16 keys of P = 8 TMEM columns
+          mma_ts_w_off<boff, acol>(dt, at, vd, idesc_pv, kk > 0 ? 1u : accumulate);
+        });
       };
 
-      for (int r = 0; ok && r * G < p.n_units; ++r) {
-        const int u = unit_of(r, cta, G);
-        if (u >= p.n_units) continue;
-        const Unit w = decode_unit(p, u);
-        if (w.nkv == 0) continue;
+      UnitIter it;
+      it.begin(p, cta, G);
+      for (; ok && it.u >= 0; it.advance(p, cta, G)) {
+        const int u = it.u;
+        const Unit w = decode_unit(p, u, it.kl_raw);
+        if (w.nkv == 0) continue;  // (advance requests the next unit)
         auto kslot = [&](int j) { return (g + 2u * j) % C::STAGES; };
         auto kphase = [&](int j) { return ((g + 2u * j) / C::STAGES) & 1u; };
         auto vslot = [&](int j) { return (g + 2u * j + 1u) % C::STAGES; };
@@ -452,11 +523,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         mma_commit_w(bar(C::B_KV_EMPTY + kslot(0)));
 
-        const uint8_t* modes = p.v_mode + (size_t)w.bh * p.n_kv_tiles;
-        int vmode_next = __ldg(modes);
+        const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride;
+        int vmode_next = it.mode0;
         for (int j = 0; ok && j < w.nkv; ++j) {
           const uint32_t idesc_pv = vmode_next == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
           if (j + 1 < w.nkv) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+          it.at_tile(p, j);
           // V_j and K_j+1 are almost always resident already: check both before
           // waiting on P, so that P's arrival is followed by back-to-back MMAs.
           ok = wait_bar(waiter, bar(C::B_KV_FULL + vslot(j)), vphase(j), C::B_KV_FULL + vslot(j), u);
@@ -528,10 +600,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
 
-    for (int r = 0; ok && r * G < p.n_units; ++r) {
-      const int u = unit_of(r, cta, G);
-      if (u >= p.n_units) continue;
-      const Unit w = decode_unit(p, u);
+    UnitIter it;
+    it.begin(p, cta, G);
+    for (; ok && it.u >= 0; it.advance(p, cta, G)) {
+      const int u = it.u;
+      const Unit w = decode_unit(p, u, it.kl_raw);
       if (!w.valid(t)) continue;
       const int n_t = w.n(t);
       const int min_lim = w.min_lim(t);
@@ -551,42 +624,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int lim = p.causal ? min(w.kl, row + 1) : w.kl;  // keys [0, lim) are visible
       float m_ref = -INFINITY;
       float l = 0.0f;
-      const uint8_t* modes = p.v_mode + (size_t)w.bh * p.n_kv_tiles;
-      int vmode_next = __ldg(modes);
+      const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride;
+      int vmode_next = it.mode0;
 
       for (int j = 0; j < n_t; ++j) {
         const int vmode = vmode_next;
         if (j + 1 < n_t) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+        it.at_tile(p, j);
         ok = wait_bar(waiter, bar_s_full, s_cnt & 1u, C::B_S_FULL + t, u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ++s_cnt;
         tc_fence_after();
 
-        float s[BN];  // this row of S, for the row max only
-        {
-          uint32_t r32[BN];
-          tmem_ld128(s_addr, r32);
-          tmem_ld_wait(r32);
-#pragma unroll
-          for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r32[i]);
-        }
         const bool masked_tile = (j + 1) * BN > min_lim;
         const int vis_n = lim - j * BN;  // columns [0, vis_n) visible
-        if (masked_tile) {
+        // row max: from the TMEM load's max reduction on tiles without a mask;
+        // with a mask, in registers over the visible columns only
+        float mx;
+        if (!masked_tile) {
+          float m0, m1;
+          {
+            float sr[64];
+            tmem_ld64_max(s_addr, sr, m0);
+            tmem_ld_wait(sr, m0);
+          }
+          {
+            float sr[64];
+            tmem_ld64_max(s_addr + 64u, sr, m1);
+            tmem_ld_wait(sr, m1);
+          }
+          mx = fmaxf(m0, m1);
+        } else {
+          float s[BN];
+          {
+            uint32_t r32[BN];
+            tmem_ld128(s_addr, r32);
+            tmem_ld_wait(r32);
 #pragma unroll
-          for (int i = 0; i < BN; ++i) s[i] = i < vis_n ? s[i] : -INFINITY;
+            for (int i = 0; i < BN; ++i) s[i] = i < vis_n ? __uint_as_float(r32[i]) : -INFINITY;
+          }
+          float mx8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(s[i], s[i + 8], s[i + 16]);
+#pragma unroll
+          for (int i = 24; i < BN; i += 16) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[i + k], i + 8 + k < BN ? s[i + 8 + k] : -INFINITY);
+          }
+          mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         }
-        // row max: 8 independent chains of 3-input max
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(s[i], s[i + 8], s[i + 16]);
-#pragma unroll
-        for (int i = 24; i < BN; i += 16) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[i + k], i + 8 + k < BN ? s[i + 8 + k] : -INFINITY);
-        }
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         const float m_new = fmaxf(m_ref, mx);
         float alpha = 1.0f;
         bool rescale = false;
@@ -672,30 +759,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++o_cnt;
       tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+      // read O 64 columns at a time, pack to bf16 and store each half; O is
+      // handed back to the MMA issuer once both halves are in registers
+      uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r32[32];
-        tmem_ld32(o_addr + 32u * cc, r32);
-        tmem_ld_wait(r32);
+      for (int hcol = 0; hcol < D / 64; ++hcol) {
+        uint32_t ov[64];
+        tmem_ld64(o_addr + 64u * hcol, ov);
+        tmem_ld_wait(ov);
+        uint32_t ob[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          ob[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+        if (hcol == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar_o_empty);
+        }
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D + 32 * cc);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r32[8 * i + 0]) * inv_l, __uint_as_float(r32[8 * i + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(r32[8 * i + 2]) * inv_l, __uint_as_float(r32[8 * i + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(r32[8 * i + 4]) * inv_l, __uint_as_float(r32[8 * i + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(r32[8 * i + 6]) * inv_l, __uint_as_float(r32[8 * i + 7]) * inv_l);
-            dst[i] = v;
-          }
+          for (int i = 0; i < 8; ++i) dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
         }
       }
       if (row_ok) {
         const float lse = (l > 0.0f) ? (m_ref * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         p.lse[row_flat] = lse;
       }
-      tc_fence_before();
-      mbar_arrive(bar_o_empty);
     }
   }
 

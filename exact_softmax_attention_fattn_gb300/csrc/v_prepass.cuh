@@ -24,7 +24,7 @@ constexpr int PREPASS_THREADS = 256;
 template <int D>
 __global__ void __launch_bounds__(PREPASS_THREADS)
     fattn_v_prepass_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, uint8_t* __restrict__ mode, int N,
-                           int n_tiles) {
+                           int n_tiles, int mode_stride) {
   constexpr int VEC = 8;                                  // bf16 per 16-byte vector
   constexpr int PER = BN * D / VEC / PREPASS_THREADS;     // vectors per thread
   const long long tile_id = blockIdx.x;
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(PREPASS_THREADS)
       v16[base + idx] = o;
     }
   }
-  if (threadIdx.x == 0) mode[bh * n_tiles + tile] = to_f16 ? VMODE_F16 : VMODE_BF16;
+  if (threadIdx.x == 0) mode[bh * mode_stride + tile] = to_f16 ? VMODE_F16 : VMODE_BF16;
 }
 
 }  // namespace fattn

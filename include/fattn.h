@@ -122,7 +122,8 @@ FATTN_API int fattn_last_error(void* stream, int* detail);
  * library, and calls no cudaMalloc, cudaFree or allocating routine.
  *
  *   - Limit: the problem must fit the array:
- *       round_up(B*H*N*d*2, 256) + round_up(B*H*ceil(N/128), 256) <= 64 MiB
+ *       round_up(B*H*N*d*2, 256) + round_up(B*H*round_up(ceil(N/128), 8), 256)
+ *         <= 64 MiB
  *     (for example B*H <= 63 at N = 4096, d = 128); larger problems return
  *     FATTN_ERR_UNSUPPORTED before anything is enqueued.
  *   - Set-up: the first call on a device (with that device current) looks up
