@@ -102,10 +102,9 @@ struct Cfg {
   static constexpr int B_O_FULL = 8;                     // [2]
   static constexpr int B_O_EMPTY = 10;                   // [2]
   static constexpr int B_DRAIN = 12;                     // [1]
-  static constexpr int B_PH_FULL = 13;                   // [2] first half of P (keys 0-63) written
-  static constexpr int B_KV_FULL = 15;                   // [STAGES]
-  static constexpr int B_KV_EMPTY = 15 + STAGES;         // [STAGES]
-  static constexpr int NUM_BARS = 15 + 2 * STAGES;
+  static constexpr int B_KV_FULL = 13;                   // [STAGES]
+  static constexpr int B_KV_EMPTY = 13 + STAGES;         // [STAGES]
+  static constexpr int NUM_BARS = 13 + 2 * STAGES;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
   static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -331,7 +330,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(C::B_P_FULL + t), BM);
       mbar_init(bar(C::B_O_FULL + t), 1);
       mbar_init(bar(C::B_O_EMPTY + t), BM);
-      mbar_init(bar(C::B_PH_FULL + t), BM);
     }
     mbar_init(bar(C::B_DRAIN), 1);
     for (int s = 0; s < C::STAGES; ++s) {
@@ -378,42 +376,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_3d(dst + pn * PANEL_BYTES, &tmap_q, bar(C::B_Q_FULL + t), 64 * pn, w.r0 + t * BM, w.bh);
         ++q_use;
       };
-      // L2 prefetch: K/V tiles PF steps ahead of the ring, and the next unit's
-      // Q tiles and first K/V tiles, so the ring's TMA loads hit L2.
-      constexpr int PF = 3;
-      auto prefetch_kv = [&](const Unit& w, int j) {
-#pragma unroll
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_prefetch_l2_3d(&tmap_k, 64 * pn, j * BN, w.bh);
-          tma_prefetch_l2_3d(&tmap_v, 64 * pn, j * BN, w.bh);
-        }
-      };
       UnitIter it;
       it.begin(p, cta, G);
-      bool first_unit = true;
       for (; ok && it.u >= 0; it.advance(p, cta, G)) {
         const int u = it.u;
         const Unit w = decode_unit(p, u, it.kl_raw);
         it.at_tile(p, it.fetch_at);
-        if (first_unit)
-          for (int j = 1; j < PF && j < w.nkv; ++j) prefetch_kv(w, j);
-        first_unit = false;
-        {
-          // the next unit this CTA will process
-          if (it.u_next >= 0) {
-            const Unit wn = decode_unit(p, it.u_next, it.kl_next);
-#pragma unroll
-            for (int t = 0; t < QT; ++t)
-              if (wn.n(t) > 0)
-#pragma unroll
-                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(&tmap_q, 64 * pn, wn.r0 + t * BM, wn.bh);
-            for (int j = 0; j < PF && j < wn.nkv; ++j) prefetch_kv(wn, j);
-          }
-        }
         load_q(TileC<0>{}, w, u, q_use0);
         load_q(TileC<1>{}, w, u, q_use1);
         for (int j = 0; ok && j < w.nkv; ++j) {
-          if (j + PF < w.nkv) prefetch_kv(w, j + PF);
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
             const uint32_t slot = g % C::STAGES;
@@ -545,18 +516,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = __all_sync(0xffffffffu, ok);
               if (!ok) return;
             }
-            // first half of P (keys 0-63), then the rest
-            ok = wait_bar(waiter, bar(C::B_PH_FULL + t), pv_cnt[t] & 1u, C::B_PH_FULL + t, u);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) return;
-            tc_fence_after();
-            issue_pv(tc, TileC<0>{}, TileC<BN / 32>{}, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
             ok = wait_bar(waiter, bar(C::B_P_FULL + t), pv_cnt[t] & 1u, C::B_P_FULL + t, u);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             ++pv_cnt[t];
             tc_fence_after();
-            issue_pv(tc, TileC<BN / 32>{}, TileC<BN / 16>{}, vslot(j), 1u, idesc_pv);
+            issue_pv(tc, TileC<0>{}, TileC<BN / 16>{}, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
             if (j == w.n(t) - 1) mma_commit_w(bar(C::B_O_FULL + t));
             if (j + 1 < w.n(t)) {
               issue_s(tc, kslot(j + 1));
@@ -593,7 +558,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t o_addr = tmem + lane_off + TMEM_O0 + 128u * t;
     const uint32_t bar_s_full = bar(C::B_S_FULL + t);
     const uint32_t bar_p_full = bar(C::B_P_FULL + t);
-    const uint32_t bar_ph_full = bar(C::B_PH_FULL + t);
     const uint32_t bar_o_full = bar(C::B_O_FULL + t);
     const uint32_t bar_o_empty = bar(C::B_O_EMPTY + t);
     const float c = p.scale_log2;
@@ -703,8 +667,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // p = 2^(s*c - m*c): kept in fp32 for l, rounded once for PV, to fp16
         // when this V tile is stored in fp16 (the usual case: 11 significant
         // bits) and to bf16 when it is not.  Masked entries are exactly zero.
-        // Each half row (64 keys) is stored and released on its own so that
-        // the P V product can start on the first half.
+        // The row is done in two halves of 64 keys, each reloaded from tensor
+        // memory, so that S and P of only one half are held in registers.
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nmc2 = f2_pack(-mc, -mc);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -729,12 +693,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             pk[q] = pack(p0, p1);
           }
           tmem_st32(s_addr + 32u * h, pk);
-          tmem_st_wait();
-          tc_fence_before();
         };
         auto both_halves = [&](auto pack) {
           half_row(0, pack);
-          mbar_arrive(bar_ph_full);
           half_row(1, pack);
         };
         if (vmode == VMODE_F16)
@@ -748,6 +709,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         f2_unpack(acc[3], a6, a7);
         const float rs = ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
         l = l * alpha + rs;
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(bar_p_full);
       }
       if (!ok) break;
