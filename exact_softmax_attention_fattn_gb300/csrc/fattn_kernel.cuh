@@ -102,9 +102,14 @@ struct Cfg {
   static constexpr int B_O_FULL = 8;                     // [2]
   static constexpr int B_O_EMPTY = 10;                   // [2]
   static constexpr int B_DRAIN = 12;                     // [1]
-  static constexpr int B_KV_FULL = 13;                   // [STAGES]
-  static constexpr int B_KV_EMPTY = 13 + STAGES;         // [STAGES]
-  static constexpr int NUM_BARS = 13 + 2 * STAGES;
+  // K/V tiles are loaded in groups, one per MMA step (see the producer);
+  // group k uses barrier pair k % KV_GROUPS.  At most STAGES groups hold ring
+  // slots at a time, so a pair is never re-armed before its last use ended.
+  static constexpr int KV_GROUPS = 2 * STAGES;
+  static_assert(KV_GROUPS <= 32, "group sizes are kept in one 32-bit mask");
+  static constexpr int B_KV_FULL = 13;                   // [KV_GROUPS]
+  static constexpr int B_KV_EMPTY = 13 + KV_GROUPS;      // [KV_GROUPS]
+  static constexpr int NUM_BARS = 13 + 2 * KV_GROUPS;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
   static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(C::B_O_EMPTY + t), BM);
     }
     mbar_init(bar(C::B_DRAIN), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < C::KV_GROUPS; ++s) {
       mbar_init(bar(C::B_KV_FULL + s), 1);
       mbar_init(bar(C::B_KV_EMPTY + s), 1);
     }
@@ -376,6 +381,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_3d(dst + pn * PANEL_BYTES, &tmap_q, bar(C::B_Q_FULL + t), 64 * pn, w.r0 + t * BM, w.bh);
         ++q_use;
       };
+      // K and V tiles go into a STAGES-deep ring of tile slots (ring position
+      // g -> slot g % STAGES), in groups read by one MMA step: a unit's first
+      // K tile alone, then (V_j, K_j+1) for each step j, the last step's V
+      // tile alone.  A group completes one full barrier (one transaction count
+      // for all its tiles) and is released by one commit, so the MMA issuer
+      // waits and commits once per step.  A slot is written again once the
+      // group holding its previous tile has been released; groups are
+      // released in order, so the positions released so far are counted.
+      uint32_t gk = 0;        // groups armed
+      uint32_t gr = 0;        // groups seen released
+      uint32_t released = 0;  // ring positions of released groups
+      uint32_t two = 0;       // bit k % 32: group k holds two tiles
+      auto make_room = [&](uint32_t pos, uint32_t groups_armed, int u) {
+        while (ok && (released + C::STAGES <= pos || groups_armed >= gr + C::KV_GROUPS)) {
+          const int id = C::B_KV_EMPTY + (int)(gr % C::KV_GROUPS);
+          ok = wait_bar(waiter, bar(id), (gr / C::KV_GROUPS) & 1u, id, u);
+          released += 1u + ((two >> (gr % 32u)) & 1u);
+          ++gr;
+        }
+      };
+      auto load_kv = [&](const CUtensorMap* map, int j, int bh, uint32_t full) {
+        const uint32_t dst = base + C::RING_OFF + (g % C::STAGES) * C::TILE_BYTES;
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn) tma_load_3d(dst + pn * PANEL_BYTES, map, full, 64 * pn, j * BN, bh);
+        ++g;
+      };
       UnitIter it;
       it.begin(p, cta, G);
       for (; ok && it.u >= 0; it.advance(p, cta, G)) {
@@ -384,30 +415,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         it.at_tile(p, it.fetch_at);
         load_q(TileC<0>{}, w, u, q_use0);
         load_q(TileC<1>{}, w, u, q_use1);
-        for (int j = 0; ok && j < w.nkv; ++j) {
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            const uint32_t slot = g % C::STAGES;
-            const uint32_t ph = (g / C::STAGES) & 1u;
-            ok = wait_bar(waiter, bar(C::B_KV_EMPTY + slot), ph ^ 1u, C::B_KV_EMPTY + slot, u);
+        // group of step j: V_j (j >= 0) and K_j+1 (j+1 < nkv); j = -1 is K_0.
+        // A unit with no key tile loads nothing (the MMA issuer skips it too).
+        for (int j = -1; ok && w.nkv > 0 && j < w.nkv; ++j) {
+          const bool has_v = j >= 0, has_k = j + 1 < w.nkv;
+          const uint32_t ntiles = (has_v ? 1u : 0u) + (has_k ? 1u : 0u);
+          make_room(g, gk, u);
+          if (!ok) break;
+          const uint32_t full = bar(C::B_KV_FULL + (int)(gk % C::KV_GROUPS));
+          mbar_arrive_expect_tx(full, ntiles * C::TILE_BYTES);
+          const uint32_t bit = 1u << (gk % 32u);
+          two = ntiles == 2u ? (two | bit) : (two & ~bit);
+          ++gk;
+          if (has_v) load_kv(&tmap_v, j, w.bh, full);
+          if (has_k) {
+            make_room(g, gk - 1u, u);
             if (!ok) break;
-            mbar_arrive_expect_tx(bar(C::B_KV_FULL + slot), C::TILE_BYTES);
-            const uint32_t dst = base + C::RING_OFF + slot * C::TILE_BYTES;
-            const CUtensorMap* map = which == 0 ? &tmap_k : &tmap_v;
-#pragma unroll
-            for (int pn = 0; pn < C::PANELS; ++pn)
-              tma_load_3d(dst + pn * PANEL_BYTES, map, bar(C::B_KV_FULL + slot), 64 * pn, j * BN, w.bh);
-            ++g;
+            load_kv(&tmap_k, j + 1, w.bh, full);
           }
         }
       }
-      // Drain: wait (bounded) for every copy that may still be in flight -- after
-      // an abort anywhere in the CTA they may never have been consumed.  Loads
-      // older than the last STAGES were consumed before their slot was reused;
+      // Drain: wait (bounded) for every group that may still have copies in
+      // flight -- after an abort anywhere in the CTA they may never have been
+      // consumed.  A barrier pair is re-armed only after its previous group
+      // was released, so the last KV_GROUPS groups are the ones still tracked;
       // in a normal run every phase below has already completed.
-      const uint32_t first = g > (uint32_t)C::STAGES ? g - C::STAGES : 0u;
-      for (uint32_t gi = first; gi < g; ++gi)
-        drain_wait(bar(C::B_KV_FULL + gi % C::STAGES), (gi / C::STAGES) & 1u, 20000000ull);
+      const uint32_t first = gk > (uint32_t)C::KV_GROUPS ? gk - C::KV_GROUPS : 0u;
+      for (uint32_t k = first; k < gk; ++k)
+        drain_wait(bar(C::B_KV_FULL + (int)(k % C::KV_GROUPS)), (k / C::KV_GROUPS) & 1u, 20000000ull);
       if (q_use0) drain_wait(bar(C::B_Q_FULL + 0), (q_use0 - 1) & 1u, 20000000ull);
       if (q_use1) drain_wait(bar(C::B_Q_FULL + 1), (q_use1 - 1) & 1u, 20000000ull);
     }
@@ -421,7 +456,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t IDESC_S = idesc_f16kind(BM, BN, true, false);      // Q, K bf16
       constexpr uint32_t IDESC_PV_F16 = idesc_f16kind(BM, D, false, true);  // P, V f16; V MN-major
       constexpr uint32_t IDESC_PV_BF16 = idesc_f16kind(BM, D, true, true);  // P, V bf16; V MN-major
-      uint32_t g = 0;  // ring position consumed
+      uint32_t g = 0;   // ring position consumed
+      uint32_t gm = 0;  // K/V groups consumed
       uint32_t q_use[QT] = {0, 0};
       uint32_t units_done[QT] = {0, 0};
       uint32_t pv_cnt[QT] = {0, 0};
@@ -469,13 +505,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Unit w = decode_unit(p, u, it.kl_raw);
         if (w.nkv == 0) continue;  // (advance requests the next unit)
         auto kslot = [&](int j) { return (g + 2u * j) % C::STAGES; };
-        auto kphase = [&](int j) { return ((g + 2u * j) / C::STAGES) & 1u; };
         auto vslot = [&](int j) { return (g + 2u * j + 1u) % C::STAGES; };
-        auto vphase = [&](int j) { return ((g + 2u * j + 1u) / C::STAGES) & 1u; };
+
+        // K/V group gm: one full barrier for the tiles of one step
+        auto kv_wait = [&]() {
+          const int id = C::B_KV_FULL + (int)(gm % C::KV_GROUPS);
+          ok = wait_bar(waiter, bar(id), (gm / C::KV_GROUPS) & 1u, id, u);
+          ok = __all_sync(0xffffffffu, ok);
+        };
+        auto kv_release = [&]() {
+          mma_commit_w(bar(C::B_KV_EMPTY + (int)(gm % C::KV_GROUPS)));
+          ++gm;
+        };
 
         // prologue: S_t,0 for each tile with work
-        ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(0)), kphase(0), C::B_KV_FULL + kslot(0), u);
-          ok = __all_sync(0xffffffffu, ok);
+        kv_wait();
         issued_any = true;  // before any MMA, so an abort mid-prologue still drains
         auto prologue = [&](auto tc) {
           constexpr int t = decltype(tc)::value;
@@ -492,7 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prologue(TileC<0>{});
         prologue(TileC<1>{});
         if (!ok) break;
-        mma_commit_w(bar(C::B_KV_EMPTY + kslot(0)));
+        kv_release();
 
         const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride;
         int vmode_next = it.mode0;
@@ -500,13 +544,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t idesc_pv = vmode_next == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
           if (j + 1 < w.nkv) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
           it.at_tile(p, j);
-          // V_j and K_j+1 are almost always resident already: check both before
-          // waiting on P, so that P's arrival is followed by back-to-back MMAs.
-          ok = wait_bar(waiter, bar(C::B_KV_FULL + vslot(j)), vphase(j), C::B_KV_FULL + vslot(j), u);
-          ok = __all_sync(0xffffffffu, ok);
-          if (ok && j + 1 < w.nkv)
-            ok = wait_bar(waiter, bar(C::B_KV_FULL + kslot(j + 1)), kphase(j + 1), C::B_KV_FULL + kslot(j + 1), u);
-          ok = __all_sync(0xffffffffu, ok);
+          // V_j and K_j+1 (almost always resident already), before waiting on P
+          kv_wait();
           // O_t += P_t V_j, then S_t,j+1 = Q_t K_j+1^T (tile 1's MMAs run while tile 0's softmax works)
           auto step = [&](auto tc) {
             constexpr int t = decltype(tc)::value;
@@ -532,8 +571,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           step(TileC<0>{});
           step(TileC<1>{});
           if (!ok) break;
-          mma_commit_w(bar(C::B_KV_EMPTY + vslot(j)));
-          if (j + 1 < w.nkv) mma_commit_w(bar(C::B_KV_EMPTY + kslot(j + 1)));
+          kv_release();
         }
         g += 2u * (uint32_t)w.nkv;
         if (w.n0 > 0) ++units_done[0];
