@@ -508,10 +508,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         auto vslot = [&](int j) { return (g + 2u * j + 1u) % C::STAGES; };
 
         // K/V group gm: one full barrier for the tiles of one step
+        // (no vote after the waits of the step loop: every lane tests the same
+        // barrier word in the same instruction, so the result is warp-uniform)
         auto kv_wait = [&]() {
           const int id = C::B_KV_FULL + (int)(gm % C::KV_GROUPS);
           ok = wait_bar(waiter, bar(id), (gm / C::KV_GROUPS) & 1u, id, u);
-          ok = __all_sync(0xffffffffu, ok);
         };
         auto kv_release = [&]() {
           mma_commit_w(bar(C::B_KV_EMPTY + (int)(gm % C::KV_GROUPS)));
@@ -556,7 +557,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (!ok) return;
             }
             ok = wait_bar(waiter, bar(C::B_P_FULL + t), pv_cnt[t] & 1u, C::B_P_FULL + t, u);
-            ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             ++pv_cnt[t];
             tc_fence_after();
@@ -702,9 +702,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
 
-        // p = 2^(s*c - m*c): kept in fp32 for l, rounded once for PV, to fp16
-        // when this V tile is stored in fp16 (the usual case: 11 significant
-        // bits) and to bf16 when it is not.  Masked entries are exactly zero.
+        // p = 2^(s*c - m*c): kept in fp32 for l, rounded for PV to fp16 (11
+        // significant bits), the type of the V tile in the usual case.  Where
+        // the V tile is stored in bf16, the packed P is rewritten as bf16 after
+        // both halves are stored (a short, rarely run pass; p <= 1, so fp16
+        // cannot overflow, and values under 2^-24 of the row max drop to zero).
+        // Masked entries are exactly zero.
         // The row is done in two halves of 64 keys, each reloaded from tensor
         // memory, so that S and P of only one half are held in registers.
         const uint64_t c2 = f2_pack(c, c);
@@ -736,10 +739,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           half_row(0, pack);
           half_row(1, pack);
         };
-        if (vmode == VMODE_F16)
-          both_halves([](float a, float b) { return pack_f16x2(a, b); });
-        else
-          both_halves([](float a, float b) { return pack_bf16x2(a, b); });
+        both_halves([](float a, float b) { return pack_f16x2(a, b); });
+        if (vmode != VMODE_F16) {
+          tmem_st_wait();  // the fp16 P must be in tensor memory before it is read back
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+            tmem_ld32(s_addr + 32u * h, pk);
+            tmem_ld_wait(pk);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) pk[q] = f16x2_to_bf16x2(pk[q]);
+            tmem_st32(s_addr + 32u * h, pk);
+          }
+        }
         float a0, a1, a2, a3, a4, a5, a6, a7;
         f2_unpack(acc[0], a0, a1);
         f2_unpack(acc[1], a2, a3);

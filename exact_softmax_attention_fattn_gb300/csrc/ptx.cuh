@@ -369,4 +369,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Packed f16x2 -> packed bf16x2 (each half widened exactly, then rounded to
+// nearest even).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2) {
+  uint32_t r;
+  asm("{\n\t.reg .f16 lo, hi;\n\t.reg .f32 flo, fhi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.f32.f16 flo, lo;\n\t"
+      "cvt.f32.f16 fhi, hi;\n\t"
+      "cvt.rn.bf16x2.f32 %0, fhi, flo;\n\t}"
+      : "=r"(r)
+      : "r"(h2));
+  return r;
+}
+
 }  // namespace fattn
