@@ -236,3 +236,217 @@ int fattn_oracle_probs(const uint16_t *q, const uint16_t *k, int64_t B, int64_t 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward pass (gradients of a scalar loss L through O), plain fp64.
+ *
+ * "understand-flashattention", section "Attention forward and backward
+ * formulas", backward pass, steps 1-5, with the scale of S = scale * Q K^T
+ * carried through the chain rule (it multiplies dQ and dK once):
+ *   dV   = P^T dO                                      (step 1)
+ *   dP   = dO V^T                                      (step 2)
+ *   dS_ij = P_ij (dP_ij - sum_k dP_ik P_ik)            (step 3, the row form)
+ *   dQ   = scale * dS K                                (step 4)
+ *   dK   = scale * dS^T Q                              (step 5)
+ * P is the forward's softmax of the masked, scaled scores (same definition as
+ * fattn_oracle_forward); masked entries have P = 0 and so contribute nothing.
+ * A row with no visible key has P = 0: its dQ row is 0 and it adds nothing to
+ * dK or dV.
+ *
+ * Threads: whole heads per worker when there are at least as many heads as
+ * workers; otherwise the rows of each head are split over the workers, each
+ * with private dK / dV accumulators that are summed after the join.
+ */
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int64_t H, N, d;
+    double scale;
+    int causal;
+    const int32_t *key_len;
+    const int64_t *heads;   /* flat b*H + h of each requested head */
+    int64_t n_heads;
+    double *dq, *dk, *dv;   /* [n_heads, N, d] */
+    int64_t head_begin, head_end;  /* whole-head mode: this worker's heads */
+    int64_t head, row_begin, row_end;  /* row mode: one head, this worker's rows */
+    double *dk_priv, *dv_priv;  /* row mode: private [N, d] accumulators */
+    int row_mode;
+    int status;
+} bwd_job;
+
+/* Rows [r0, r1) of head slot `hs` (flat head bh): dQ rows into dq_head,
+ * dK / dV contributions added into dk_acc / dv_acc ([N, d]). */
+static void bwd_rows(const bwd_job *J, int64_t hs, int64_t r0, int64_t r1, double *dk_acc, double *dv_acc,
+                     double *s, double *p, double *dp, double *qrow, double *grow)
+{
+    const int64_t N = J->N, d = J->d;
+    const int64_t bh = J->heads ? J->heads[hs] : hs;
+    const int64_t b = bh / J->H;
+    const uint16_t *qp = J->q + bh * N * d;
+    const uint16_t *kp = J->k + bh * N * d;
+    const uint16_t *vp = J->v + bh * N * d;
+    const uint16_t *gp = J->dout + bh * N * d;
+    double *dq_head = J->dq + hs * N * d;
+    int64_t klen = N;
+    if (J->key_len) {
+        klen = J->key_len[b];
+        if (klen < 0) klen = 0;
+        if (klen > N) klen = N;
+    }
+    for (int64_t i = r0; i < r1; ++i) {
+        for (int64_t t = 0; t < d; ++t) {
+            qrow[t] = bf16_bits_to_double(qp[i * d + t]);
+            grow[t] = bf16_bits_to_double(gp[i * d + t]);
+        }
+        /* forward: scaled scores, visibility, softmax row */
+        int any = 0;
+        double m = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc += qrow[t] * bf16_bits_to_double(kp[j * d + t]);
+            s[j] = J->scale * acc;
+            int vis = (!J->causal || j <= i) && j < klen;
+            if (vis && (!any || s[j] > m)) m = s[j];
+            if (vis) any = 1;
+        }
+        double *dqi = dq_head + i * d;
+        for (int64_t t = 0; t < d; ++t) dqi[t] = 0.0;
+        if (!any) continue;
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            int vis = (!J->causal || j <= i) && j < klen;
+            p[j] = vis ? exp(s[j] - m) : 0.0;
+            l += p[j];
+        }
+        for (int64_t j = 0; j < N; ++j) p[j] /= l;
+        /* step 2: dP row = dO_i . v_j */
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc += grow[t] * bf16_bits_to_double(vp[j * d + t]);
+            dp[j] = acc;
+        }
+        /* step 3: dS_ij = P_ij (dP_ij - sum_k dP_ik P_ik) */
+        double r = 0.0;
+        for (int64_t j = 0; j < N; ++j) r += dp[j] * p[j];
+        for (int64_t j = 0; j < N; ++j) {
+            if (p[j] == 0.0) continue;
+            const double ds = p[j] * (dp[j] - r);
+            const uint16_t *kj = kp + j * d;
+            for (int64_t t = 0; t < d; ++t) {
+                dqi[t] += J->scale * ds * bf16_bits_to_double(kj[t]);  /* step 4 */
+                dk_acc[j * d + t] += J->scale * ds * qrow[t];          /* step 5 */
+                dv_acc[j * d + t] += p[j] * grow[t];                   /* step 1 */
+            }
+        }
+    }
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *J = (bwd_job *)arg;
+    const int64_t N = J->N, d = J->d;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(3 * N + 2 * d));
+    if (!s) {
+        J->status = 2;
+        return NULL;
+    }
+    double *p = s + N, *dp = p + N, *qrow = dp + N, *grow = qrow + d;
+    if (J->row_mode) {
+        bwd_rows(J, J->head, J->row_begin, J->row_end, J->dk_priv, J->dv_priv, s, p, dp, qrow, grow);
+    } else {
+        for (int64_t hs = J->head_begin; hs < J->head_end; ++hs) {
+            double *dk = J->dk + hs * N * d, *dv = J->dv + hs * N * d;
+            for (int64_t x = 0; x < N * d; ++x) dk[x] = dv[x] = 0.0;
+            bwd_rows(J, hs, 0, N, dk, dv, s, p, dp, qrow, grow);
+        }
+    }
+    free(s);
+    J->status = 0;
+    return NULL;
+}
+
+/*
+ * q, k, v, dout : bf16 bits, [B, H, N, d] contiguous (dout = dL/dO).
+ * key_len       : int32 [B] or NULL.
+ * heads         : flat b*H + h of the heads to evaluate, or NULL for all B*H.
+ * dq, dk, dv    : double [n_heads, N, d] (n_heads = B*H when heads is NULL).
+ * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ */
+int fattn_oracle_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
+                          int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                          const int32_t *key_len, const int64_t *heads, int64_t n_heads,
+                          double *dq, double *dk, double *dv, int n_threads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H < 0 || N < 0 || d <= 0) return 1;
+    if (!heads) n_heads = B * H;
+    if (n_heads < 0) return 1;
+    if (heads)
+        for (int64_t x = 0; x < n_heads; ++x)
+            if (heads[x] < 0 || heads[x] >= B * H) return 1;
+    if (n_heads == 0 || N == 0) return 0;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+
+    bwd_job proto;
+    memset(&proto, 0, sizeof proto);
+    proto.q = q; proto.k = k; proto.v = v; proto.dout = dout;
+    proto.H = H; proto.N = N; proto.d = d; proto.scale = scale; proto.causal = causal;
+    proto.key_len = key_len; proto.heads = heads; proto.n_heads = n_heads;
+    proto.dq = dq; proto.dk = dk; proto.dv = dv;
+
+    bwd_job jobs[256];
+    pthread_t tids[256];
+    int started[256];
+    int rc = 0;
+    if (n_heads >= n_threads) {
+        for (int w = 0; w < n_threads; ++w) {
+            jobs[w] = proto;
+            jobs[w].head_begin = n_heads * w / n_threads;
+            jobs[w].head_end = n_heads * (w + 1) / n_threads;
+        }
+        for (int w = 0; w < n_threads; ++w) {
+            started[w] = (n_threads > 1) && pthread_create(&tids[w], NULL, bwd_worker, &jobs[w]) == 0;
+            if (!started[w]) bwd_worker(&jobs[w]);
+        }
+        for (int w = 0; w < n_threads; ++w) {
+            if (started[w]) pthread_join(tids[w], NULL);
+            if (jobs[w].status) rc = jobs[w].status;
+        }
+        return rc;
+    }
+    int nw = n_threads;
+    if ((int64_t)nw > N) nw = (int)N;
+    double *priv = (double *)malloc(sizeof(double) * (size_t)(2 * nw) * (size_t)(N * d));
+    if (!priv) return 2;
+    for (int64_t hs = 0; hs < n_heads && rc == 0; ++hs) {
+        for (int w = 0; w < nw; ++w) {
+            jobs[w] = proto;
+            jobs[w].row_mode = 1;
+            jobs[w].head = hs;
+            jobs[w].row_begin = N * w / nw;
+            jobs[w].row_end = N * (w + 1) / nw;
+            jobs[w].dk_priv = priv + (size_t)(2 * w) * (size_t)(N * d);
+            jobs[w].dv_priv = jobs[w].dk_priv + N * d;
+            for (int64_t x = 0; x < 2 * N * d; ++x) jobs[w].dk_priv[x] = 0.0;
+        }
+        for (int w = 0; w < nw; ++w) {
+            started[w] = (nw > 1) && pthread_create(&tids[w], NULL, bwd_worker, &jobs[w]) == 0;
+            if (!started[w]) bwd_worker(&jobs[w]);
+        }
+        for (int w = 0; w < nw; ++w) {
+            if (started[w]) pthread_join(tids[w], NULL);
+            if (jobs[w].status) rc = jobs[w].status;
+        }
+        double *dkh = dk + hs * N * d, *dvh = dv + hs * N * d;
+        for (int64_t x = 0; x < N * d; ++x) {
+            double a = 0.0, c = 0.0;
+            for (int w = 0; w < nw; ++w) {
+                a += jobs[w].dk_priv[x];
+                c += jobs[w].dv_priv[x];
+            }
+            dkh[x] = a;
+            dvh[x] = c;
+        }
+    }
+    free(priv);
+    return rc;
+}

@@ -1,4 +1,4 @@
-"""Plain fp64 CPU oracle for the exact softmax attention forward.
+"""Plain fp64 CPU oracle for the exact softmax attention forward and backward.
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 benchmark's CPU-baseline / reference leg import this module.  The product path
@@ -47,6 +47,13 @@ def _bind(path: str):
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
+    lib.fattn_oracle_backward.restype = ctypes.c_int
+    lib.fattn_oracle_backward.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
     ]
     lib.fattn_oracle_probs.restype = ctypes.c_int
     lib.fattn_oracle_probs.argtypes = [
@@ -119,6 +126,49 @@ def forward(q, k, v, scale: float, causal: bool, key_len=None, rows=None, thread
     return o, lse
 
 
+def backward(q, k, v, dout, scale: float, causal: bool, key_len=None, heads=None, threads: int | None = None,
+             _lib_override=None):
+    """Exact attention backward in fp64: (dQ, dK, dV) for the loss gradient dout = dL/dO.
+
+    q, k, v, dout: uint16 bf16 bit patterns, shape [B, H, N, d].  key_len:
+    int32 [B] or None.  heads: optional flat head ids b*H+h; the result then
+    has shape [len(heads), N, d] per tensor, else [B, H, N, d].
+
+    Follows "understand-flashattention", section "Attention forward and
+    backward formulas", backward pass steps 1-5 (dV = P^T dO, dP = dO V^T,
+    dS_ij = P_ij (dP_ij - sum_k dP_ik P_ik), dQ = dS K, dK = dS^T Q), with the
+    softmax scale of S = scale * Q K^T carried into dQ and dK by the chain rule,
+    and P the forward's masked softmax (forward()).
+    """
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q, k, v, dout must share the shape [B, H, N, d]")
+    B, H, N, d = q.shape
+    kl = None
+    if key_len is not None:
+        kl = np.ascontiguousarray(key_len, dtype=np.int32)
+        if kl.shape != (B,):
+            raise ValueError("key_len must have shape [B]")
+    hs = None
+    if heads is not None:
+        hs = np.ascontiguousarray(heads, dtype=np.int64)
+        n_heads = hs.size
+        shape = (n_heads, N, d)
+    else:
+        n_heads = B * H
+        shape = (B, H, N, d)
+    dq = np.empty(shape, dtype=np.float64)
+    dk = np.empty(shape, dtype=np.float64)
+    dv = np.empty(shape, dtype=np.float64)
+    rc = (_lib_override or _load()).fattn_oracle_backward(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, H, N, d, float(scale),
+        int(bool(causal)), kl.ctypes.data if kl is not None else None, hs.ctypes.data if hs is not None else None,
+        n_heads, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle backward failed with code {rc}")
+    return dq, dk, dv
+
+
 def probs(q, k, scale: float, causal: bool, key_len=None, b: int = 0, h: int = 0, _lib_override=None):
     """The full P (softmax of the masked, scaled scores) and S of one head, fp64.
 
@@ -151,6 +201,9 @@ class Oracle:
 
     def probs(self, *a, **kw):
         return probs(*a, _lib_override=self._lib, **kw)
+
+    def backward(self, *a, **kw):
+        return backward(*a, _lib_override=self._lib, **kw)
 
 
 def compile_source(src_path: str, out_path: str) -> str:
