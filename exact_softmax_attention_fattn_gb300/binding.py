@@ -1,7 +1,8 @@
 """Thin ctypes binding over libfattn.so (include/fattn.h).
 
 Argument marshalling only: every step of the attention forward runs in the
-CUDA kernel behind `fattn_fwd`.  PyTorch supplies device memory and the
+CUDA kernel behind `fattn_fwd`, every step of the backward in the kernels
+behind `fattn_bwd`.  PyTorch supplies device memory and the
 current stream.  If the library is not built, or no GPU is present, calls
 raise FattnError: there is no fallback path.
 """
@@ -21,7 +22,7 @@ FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
-EXPORTED = ("fattn_fwd", "fattn_status_string", "fattn_last_error", "fattn_version")
+EXPORTED = ("fattn_fwd", "fattn_bwd", "fattn_status_string", "fattn_last_error", "fattn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +59,11 @@ def load_library():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_void_p,
             ]
+            lib.fattn_bwd.restype = ctypes.c_int
+            lib.fattn_bwd.argtypes = [ctypes.c_void_p] * 9 + [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p,
+            ]
             lib.fattn_status_string.restype = ctypes.c_char_p
             lib.fattn_status_string.argtypes = [ctypes.c_int]
             lib.fattn_last_error.restype = ctypes.c_int
@@ -77,6 +83,14 @@ def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int
     """fattn_fwd with raw addresses; returns the status code."""
     return load_library().fattn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                                     float(scale), int(bool(causal)), key_len_ptr, stream)
+
+
+def bwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, do_ptr: int, lse_ptr: int, dq_ptr: int, dk_ptr: int,
+            dv_ptr: int, B: int, H: int, N: int, d: int, scale: float, causal: bool, key_len_ptr: int | None,
+            stream: int | None) -> int:
+    """fattn_bwd with raw addresses; returns the status code."""
+    return load_library().fattn_bwd(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, int(B),
+                                    int(H), int(N), int(d), float(scale), int(bool(causal)), key_len_ptr, stream)
 
 
 def last_error(stream=None) -> tuple[int, list[int]]:
@@ -131,6 +145,43 @@ def forward_into(q, k, v, o, lse, causal: bool = False, scale: float | None = No
                      causal, kl_ptr, handle)
     if st != FATTN_OK:
         raise FattnError(st, "fattn_fwd")
+
+
+def backward_into(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = False, scale: float | None = None,
+                  key_len=None, stream=None) -> None:
+    """Gradients of the forward on device tensors: writes dq, dk, dv (bf16, shaped
+    like q) from dout = dL/dO and the forward's o and lse; enqueued on `stream`."""
+    import torch
+
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    for name, t in (("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    kl_ptr = None
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or key_len.shape != (B,) or key_len.device != q.device:
+            raise ValueError("key_len must be an int32 tensor [B] on q's device")
+        kl_ptr = key_len.data_ptr()
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q.device):
+        handle = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+        st = bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, causal, kl_ptr, handle)
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_bwd")
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, key_len=None):
+    """dQ, dK, dV of bf16 [B, H, N, d] device tensors (enqueued on the current stream)."""
+    import torch
+
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    backward_into(q, k, v, o, lse, dout, dq, dk, dv, causal=causal, scale=scale, key_len=key_len)
+    return dq, dk, dv
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=None):

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/fattn.h"
+#include "fattn_bwd.cuh"
 #include "fattn_kernel.cuh"
 #include "v_prepass.cuh"
 
@@ -62,6 +63,11 @@ int configure_kernel() {
   cudaFuncAttributes a;
   if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D>) != cudaSuccess) return FATTN_ERR_CUDA;
   if (a.numRegs != fattn::LAUNCH_REGS) return FATTN_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(fattn::fattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fattn::BwdCfg<D>::SMEM_BYTES) != cudaSuccess ||
+      cudaFuncSetAttribute(fattn::fattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)fattn::BwdCfg<D>::SMEM_BYTES) != cudaSuccess)
+    return FATTN_ERR_CUDA;
   return FATTN_OK;
 }
 
@@ -231,6 +237,94 @@ extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, 
   }
   rc = d == 64 ? enqueue<64>(q, k, v, p, scratch, grid, s) : enqueue<128>(q, k, v, p, scratch, grid, s);
   if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
+  return rc;
+}
+
+// ------------------------------------------------------------------------
+// fattn_bwd: gradients dQ, dK, dV from dO, the forward's O and LSE.
+namespace {
+
+template <int D>
+int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                fattn::BwdParams p, float* rows, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  const long long n_rows = (long long)BH * p.N_pad;
+  float* lse2 = rows;
+  float* delta = rows + n_rows;
+  p.lse2 = lse2;
+  p.delta = delta;
+  const long long prep_threads = n_rows * (D / 8);
+  fattn::fattn_bwd_prep_kernel<D>
+      <<<(unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS), fattn::PREP_THREADS, 0, stream>>>(
+          reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad,
+          n_rows);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo;
+  if (encode_map(&mq, q, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mv, v, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mdo, dout, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
+    return FATTN_ERR_CUDA;
+  const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
+  fattn::fattn_bwd_dkdv_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo,
+                                                                                                      p);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  fattn::fattn_bwd_dq_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                   float scale, int causal, const int32_t* key_len, void* stream) {
+  // ---- synchronous argument checks: nothing is enqueued on failure
+  if (B < 0 || H < 0 || N < 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
+  const void* ptrs16[8] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void* ptr : ptrs16)
+    if (!aligned(ptr, 16) || !is_device_pointer(ptr)) return FATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !is_device_pointer(lse)) return FATTN_ERR_INVALID_ARG;
+  if (key_len && (!aligned(key_len, 4) || !is_device_pointer(key_len))) return FATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  int rc = device_state(dev, &ds);
+  if (rc != FATTN_OK) return rc;
+
+  fattn::BwdParams p;
+  p.dq = reinterpret_cast<__nv_bfloat16*>(dq);
+  p.dk = reinterpret_cast<__nv_bfloat16*>(dk);
+  p.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+  p.key_len = key_len;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.n_tiles = (N + 127) / 128;
+  p.N_pad = p.n_tiles * 128;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.wait_limit_ns = wait_limit_ns();
+  p.lse2 = nullptr;
+  p.delta = nullptr;
+  if ((long long)B * H * p.n_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* rows = nullptr;
+  const size_t row_bytes = 2u * (size_t)B * (size_t)H * (size_t)p.N_pad * sizeof(float);
+  if (cudaMallocFromPoolAsync(&rows, row_bytes, ds->pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  float* rf = reinterpret_cast<float*>(rows);
+  rc = d == 64 ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s) : enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s);
+  if (cudaFreeAsync(rows, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }
 

@@ -1,0 +1,594 @@
+// Exact softmax attention backward, sm_103a.
+//
+// What it computes ("understand-flashattention", section "Attention forward
+// and backward formulas", backward pass steps 1-5, with P recomputed from the
+// saved logsumexp as in "recomputing P needs logsumexp"):
+//     P  = exp(S - LSE) with S = scale * Q K^T, masked entries 0
+//     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D) with D_i = sum_k dP_ik P_ik,
+//     dQ = scale * dS K,  dK = scale * dS^T Q.
+// D_i is computed as rowsum(dO_i * O_i), which equals sum_k dP_ik P_ik because
+// O_i = sum_k P_ik V_k.
+//
+// How (GB300):
+//   * fattn_bwd_prep_kernel: D per row and LSE * log2(e), both written to
+//     buffers whose rows are padded to a multiple of 128, so every per-tile
+//     copy of them is a 512-byte, 16-byte-aligned bulk copy for any N.
+//   * fattn_bwd_dkdv_kernel: one CTA per (batch*head, 128-key tile j).  K_j
+//     and V_j stay in shared memory; Q_i, dO_i, LSE_i, D_i stream through a
+//     two-stage ring over the query tiles i that see tile j.  Per tile:
+//     S^T = K_j Q_i^T and dP^T = V_j dO_i^T in tensor memory (lanes = keys);
+//     four warps (one thread per key) form P^T = 2^(S^T c - LSE2) and
+//     dS^T = P^T (dP^T - D), store both as bf16 over the first 64 columns of
+//     their fp32 tiles, and the MMA issuer accumulates dV += P^T dO and
+//     dK += dS^T Q in tensor memory (P^T, dS^T as the A operand from TMEM;
+//     dO, Q as MN-major B).  TMEM: S^T, dP^T, dV, dK = 4 x 128 columns.
+//   * fattn_bwd_dq_kernel: one CTA per (batch*head, 128-query tile i).  Q_i and
+//     dO_i stay; K_j, V_j stream over the key tiles i sees.  S = Q_i K_j^T,
+//     dP = dO_i V_j^T, then one thread per query row forms dS (bf16, over S)
+//     and dQ += dS K_j accumulates in tensor memory.
+//   Splitting dQ from dK/dV costs two extra GEMMs per tile pair but needs no
+//   atomics: tensor memory cannot hold S, dP, dV, dK and a dQ accumulator at
+//   d = 128.  Every wait is bounded as in the forward kernel.
+#pragma once
+
+#include "fattn_kernel.cuh"
+
+namespace fattn {
+
+constexpr int BWD_THREADS = 192;   // warps 0-3 elementwise, 4 TMA producer, 5 MMA issuer
+constexpr int BWD_PRODUCER_WARP = 4;
+constexpr int BWD_MMA_WARP = 5;
+constexpr int BWD_STAGES = 2;
+constexpr int PREP_THREADS = 256;
+
+struct BwdParams {
+  const float* lse2;    // [B*H, N_pad]: LSE * log2(e) (-inf kept; padding rows 0)
+  const float* delta;   // [B*H, N_pad]: rowsum(dO * O) (padding rows 0)
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const int32_t* key_len;  // [B] or nullptr
+  int* err;                // int[4]
+  int B, H, N, N_pad;
+  float scale;       // softmax scale (natural units)
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  int n_tiles;  // ceil(N / 128)
+  unsigned long long wait_limit_ns;
+};
+
+// ------------------------------------------------------------------ prep
+// One row per D/8 threads (16-byte loads of O and dO); rows past N (padding)
+// get D = 0 and LSE2 = 0.
+template <int D>
+__global__ void __launch_bounds__(PREP_THREADS)
+    fattn_bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout, const float* __restrict__ lse,
+                          float* __restrict__ lse2, float* __restrict__ delta, int N, int N_pad, long long n_rows) {
+  constexpr int TPR = D / 8;  // threads per row
+  const long long r = ((long long)blockIdx.x * PREP_THREADS + threadIdx.x) / TPR;
+  const int part = threadIdx.x % TPR;
+  float acc = 0.0f;
+  const long long bh = r / N_pad;
+  const int i = (int)(r % N_pad);
+  const bool live = r < n_rows && i < N;
+  if (live) {
+    const size_t at = ((size_t)bh * (size_t)N + (size_t)i) * (D / 8) + (size_t)part;
+    const uint4 a = __ldg(o + at), g = __ldg(dout + at);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      acc = fmaf(__uint_as_float(aw[x] << 16), __uint_as_float(gw[x] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[x] & 0xFFFF0000u), __uint_as_float(gw[x] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (r < n_rows && part == 0) {
+    delta[r] = live ? acc : 0.0f;
+    lse2[r] = live ? lse[(size_t)bh * (size_t)N + (size_t)i] * 1.4426950408889634f : 0.0f;
+  }
+}
+
+// ------------------------------------------------------------------ shared layout
+// Both main kernels: two stationary 128-row tiles, a BWD_STAGES ring of two
+// tiles each, and (dK/dV kernel) 512 bytes of LSE2 + 512 of D per stage.
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t TILE_BYTES = 128u * D * 2u;
+  static constexpr uint32_t FIX0_OFF = 0;                // K_j (dK/dV) or Q_i (dQ)
+  static constexpr uint32_t FIX1_OFF = TILE_BYTES;       // V_j (dK/dV) or dO_i (dQ)
+  static constexpr uint32_t RING_OFF = 2 * TILE_BYTES;   // per stage: two tiles
+  static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr uint32_t ROWS_OFF = RING_OFF + BWD_STAGES * STAGE_BYTES;  // per stage: LSE2[128], D[128]
+  static constexpr uint32_t BAR_OFF = ROWS_OFF + BWD_STAGES * 1024u;
+  // barrier ids
+  static constexpr int B_FIX_FULL = 0;
+  static constexpr int B_ST_FULL = 1;                    // [BWD_STAGES]
+  static constexpr int B_ST_EMPTY = 1 + BWD_STAGES;      // [BWD_STAGES]
+  static constexpr int B_S_FULL = 1 + 2 * BWD_STAGES;
+  static constexpr int B_DP_FULL = B_S_FULL + 1;
+  static constexpr int B_OPS_READY = B_S_FULL + 2;       // P^T / dS^T (or dS) stored
+  static constexpr int B_ACC_FULL = B_S_FULL + 3;
+  static constexpr int B_DRAIN = B_S_FULL + 4;
+  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
+  // + slack for 1024-byte alignment; at least 120 KB so that only one CTA fits
+  // an SM (each allocates all 512 TMEM columns)
+  static constexpr uint32_t SMEM_USED = MISC_OFF + 16 + 1024;
+  static constexpr uint32_t SMEM_BYTES = SMEM_USED > 120u * 1024u ? SMEM_USED : 120u * 1024u;
+};
+constexpr uint32_t BWD_TMEM_COLS = 512;
+constexpr uint32_t BT_S = 0, BT_DP = 128, BT_ACC0 = 256;  // TMEM columns; accumulators from 256
+
+// f(integral_constant<int, I>) for I = 0 .. N-1 over the MMAs of one GEMM
+// (K steps of 16): descriptor offsets are compile-time immediates.
+template <int D>
+struct BwdMma {
+  using C = BwdCfg<D>;
+  static constexpr uint32_t IDESC_KMAJOR = idesc_f16kind(128, 128, true, false);  // both operands K-major
+  static constexpr uint32_t IDESC_ACC = idesc_f16kind(128, D, true, true);        // B MN-major, N = D
+
+  // D(128 x 128) = A(128 x D) B(128 x D)^T, both K-major tiles in shared memory.
+  __device__ __forceinline__ static void ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+    static_for<D / 16>([&](auto kc) {
+      constexpr int kk = decltype(kc)::value;
+      constexpr uint32_t off = ((kk / 4) * PANEL_BYTES + (kk % 4) * 32u) >> 4;
+      mma_ss_w_off<off>(d_tmem, a_desc, b_desc, IDESC_KMAJOR, kk > 0 ? 1u : 0u);
+    });
+  }
+  // D(128 x D) (+)= A(128 x 128, bf16 in TMEM) B(128 x D, MN-major tile in shared memory).
+  __device__ __forceinline__ static void ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+    static_for<8>([&](auto kc) {
+      constexpr int kk = decltype(kc)::value;
+      constexpr uint32_t boff = (kk * 2048u) >> 4;  // 16 rows = two 1024-byte row groups
+      constexpr uint32_t acol = 8u * kk;            // 16 columns of packed bf16 = 8 TMEM columns
+      mma_ts_w_off<boff, acol>(d_tmem, a_tmem, b_desc, IDESC_ACC, kk > 0 ? 1u : accumulate);
+    });
+  }
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Rows [key0, key0 + 128) of an accumulator in TMEM -> bf16 rows of `out`
+// ([B*H, N, D]), times `mul`; rows at or past N are skipped.
+template <int D>
+__device__ __forceinline__ void store_acc_rows(uint32_t t_addr, float mul, __nv_bfloat16* out, size_t row_flat,
+                                               bool row_ok) {
+  uint4* dst = reinterpret_cast<uint4*>(out + row_flat * D);
+#pragma unroll
+  for (int hcol = 0; hcol < D / 64; ++hcol) {
+    uint32_t av[64];
+    tmem_ld64(t_addr + 64u * hcol, av);
+    tmem_ld_wait(av);
+    uint32_t ob[32];
+#pragma unroll
+    for (int x = 0; x < 32; ++x) ob[x] = pack_bf16x2(__uint_as_float(av[2 * x]) * mul, __uint_as_float(av[2 * x + 1]) * mul);
+    if (row_ok) {
+#pragma unroll
+      for (int x = 0; x < 8; ++x) dst[8 * hcol + x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void store_zero_rows(__nv_bfloat16* out, size_t row_flat, bool row_ok) {
+  if (!row_ok) return;
+  uint4* dst = reinterpret_cast<uint4*>(out + row_flat * D);
+#pragma unroll
+  for (int x = 0; x < D / 8; ++x) dst[x] = make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ int clamp_kl(const BwdParams& p, int b) {
+  int kl = p.key_len ? p.key_len[b] : p.N;
+  return kl < 0 ? 0 : (kl > p.N ? p.N : kl);
+}
+
+// ------------------------------------------------------------------ dK, dV
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fattn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                          const BwdParams p) {
+  using C = BwdCfg<D>;
+  using M = BwdMma<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  auto bar = [&](int id) -> uint32_t { return base + C::BAR_OFF + 8u * (uint32_t)id; };
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
+
+  // unit: heaviest first (under causal the first key tiles see the most queries)
+  const int BH = p.B * p.H;
+  const int jt = (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / p.H;
+  const int kl = clamp_kl(p, b);
+  const int key0 = jt * 128;
+  const int i_first = p.causal ? jt : 0;
+  const int n_q = key0 < kl ? p.n_tiles - i_first : 0;  // query tiles that see this key tile
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_FIX_FULL), 1);
+    for (int s = 0; s < BWD_STAGES; ++s) {
+      mbar_init(bar(C::B_ST_FULL + s), 1);
+      mbar_init(bar(C::B_ST_EMPTY + s), 1);
+    }
+    mbar_init(bar(C::B_S_FULL), 1);
+    mbar_init(bar(C::B_DP_FULL), 1);
+    mbar_init(bar(C::B_OPS_READY), 128);
+    mbar_init(bar(C::B_ACC_FULL), 1);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BWD_PRODUCER_WARP && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    prefetch_tensormap(&tmap_do);
+  }
+  if (warp == BWD_MMA_WARP) {
+    tmem_alloc(base + C::MISC_OFF, BWD_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_slot;
+  Waiter waiter{abort_flag, p.err, p.wait_limit_ns, 0};
+  const int u = (int)blockIdx.x;
+
+  if (n_q > 0 && warp == BWD_PRODUCER_WARP) {
+    if (lane == 0) {
+      waiter.role = ROLE_PRODUCER;
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(C::B_FIX_FULL), 2 * C::TILE_BYTES);
+#pragma unroll
+      for (int pn = 0; pn < C::PANELS; ++pn) {
+        tma_load_3d(base + C::FIX0_OFF + pn * PANEL_BYTES, &tmap_k, bar(C::B_FIX_FULL), 64 * pn, key0, bh);
+        tma_load_3d(base + C::FIX1_OFF + pn * PANEL_BYTES, &tmap_v, bar(C::B_FIX_FULL), 64 * pn, key0, bh);
+      }
+      int issued = 0;
+      for (int n = 0; ok && n < n_q; ++n) {
+        const int s = n % BWD_STAGES;
+        ok = wait_bar(waiter, bar(C::B_ST_EMPTY + s), ((n / BWD_STAGES) & 1) ^ 1, C::B_ST_EMPTY + s, u);
+        if (!ok) break;
+        const int q0 = (i_first + n) * 128;
+        const uint32_t full = bar(C::B_ST_FULL + s);
+        mbar_arrive_expect_tx(full, 2 * C::TILE_BYTES + 1024u);
+        const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+          tma_load_3d(st + pn * PANEL_BYTES, &tmap_q, full, 64 * pn, q0, bh);
+          tma_load_3d(st + C::TILE_BYTES + pn * PANEL_BYTES, &tmap_do, full, 64 * pn, q0, bh);
+        }
+        const size_t row = (size_t)bh * (size_t)p.N_pad + (size_t)q0;
+        bulk_load(base + C::ROWS_OFF + (uint32_t)s * 1024u, p.lse2 + row, 512u, full);
+        bulk_load(base + C::ROWS_OFF + (uint32_t)s * 1024u + 512u, p.delta + row, 512u, full);
+        issued = n + 1;
+      }
+      // drain: the last copies may never have been consumed after an abort
+      drain_wait(bar(C::B_FIX_FULL), 0, 20000000ull);
+      for (int n = issued > BWD_STAGES ? issued - BWD_STAGES : 0; n < issued; ++n)
+        drain_wait(bar(C::B_ST_FULL + n % BWD_STAGES), (n / BWD_STAGES) & 1, 20000000ull);
+    }
+  } else if (n_q > 0 && warp == BWD_MMA_WARP) {
+    waiter.role = ROLE_MMA;
+    bool ok = wait_bar(waiter, bar(C::B_FIX_FULL), 0, C::B_FIX_FULL, u);
+    ok = __all_sync(0xffffffffu, ok);
+    bool issued_any = false;
+    const uint64_t k_desc = smem_desc(base + C::FIX0_OFF, 16, 1024);
+    const uint64_t v_desc = smem_desc(base + C::FIX1_OFF, 16, 1024);
+    for (int n = 0; ok && n < n_q; ++n) {
+      const int s = n % BWD_STAGES;
+      ok = wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      issued_any = true;
+      tc_fence_after();
+      const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
+      M::ss(tmem + BT_S, k_desc, smem_desc(st, 16, 1024));                  // S^T = K Q^T
+      mma_commit_w(bar(C::B_S_FULL));
+      M::ss(tmem + BT_DP, v_desc, smem_desc(st + C::TILE_BYTES, 16, 1024));  // dP^T = V dO^T
+      mma_commit_w(bar(C::B_DP_FULL));
+      ok = wait_bar(waiter, bar(C::B_OPS_READY), n & 1, C::B_OPS_READY, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t acc = n > 0 ? 1u : 0u;
+      M::ts(tmem + BT_ACC0, tmem + BT_S, smem_desc(st + C::TILE_BYTES, PANEL_BYTES, 1024), acc);  // dV += P^T dO
+      M::ts(tmem + BT_ACC0 + D, tmem + BT_DP, smem_desc(st, PANEL_BYTES, 1024), acc);          // dK += dS^T Q
+      mma_commit_w(bar(C::B_ST_EMPTY + s));
+    }
+    if (ok) mma_commit_w(bar(C::B_ACC_FULL));
+    if (issued_any) {
+      mma_commit_w(bar(C::B_DRAIN));
+      drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
+    }
+  } else if (warp < 4) {
+    waiter.role = ROLE_SOFTMAX;
+    const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
+    const int key = key0 + r;
+    const bool key_vis = key < kl;
+    const size_t row_flat = (size_t)bh * (size_t)p.N + (size_t)key;
+    const bool row_ok = key < p.N;
+    if (n_q == 0) {
+      store_zero_rows<D>(p.dv, row_flat, row_ok);
+      store_zero_rows<D>(p.dk, row_flat, row_ok);
+    } else {
+      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+      const uint32_t s_addr = tmem + lane_off + BT_S;
+      const uint32_t dp_addr = tmem + lane_off + BT_DP;
+      const float c = p.scale_log2;
+      bool ok = true;
+      for (int n = 0; ok && n < n_q; ++n) {
+        const int s = n % BWD_STAGES;
+        const int q0 = (i_first + n) * 128;
+        ok = wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
+        if (ok) ok = wait_bar(waiter, bar(C::B_S_FULL), n & 1, C::B_S_FULL, u);
+        if (ok) ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float4* lse4 = reinterpret_cast<const float4*>(base_ptr + C::ROWS_OFF + (uint32_t)s * 1024u);
+        const float4* del4 = lse4 + 32;
+        // visible columns: query q0 + col sees this key iff the key is inside
+        // key_len and (causal) key <= query; rows past N read as zero and
+        // contribute nothing (their dO and Q are zero)
+        const int min_q = p.causal ? key - q0 : 0;  // columns < min_q are masked
+        const bool any_mask = !key_vis || min_q > 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sh[64], dh[64];
+          tmem_ld64(s_addr + 64u * h, sh);
+          tmem_ld64(dp_addr + 64u * h, dh);
+          tmem_ld_wait(sh);
+          tmem_ld_wait(dh);
+          uint32_t pk[32], dk2[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const float4 l4 = lse4[16 * h + q4];
+            const float4 d4 = del4[16 * h + q4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = 64 * h + 4 * q4 + e;
+              float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
+              if (any_mask) pe = (key_vis && col >= min_q) ? pe : 0.0f;
+              pv[e] = pe;
+              dsv[e] = pe * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
+            }
+            pk[2 * q4] = pack_bf16x2(pv[0], pv[1]);
+            pk[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dk2[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+            dk2[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          }
+          tmem_st32(s_addr + 32u * h, pk);
+          tmem_st32(dp_addr + 32u * h, dk2);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_OPS_READY));
+      }
+      if (ok) {
+        ok = wait_bar(waiter, bar(C::B_ACC_FULL), 0, C::B_ACC_FULL, u);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        store_acc_rows<D>(tmem + lane_off + BT_ACC0, 1.0f, p.dv, row_flat, row_ok);
+        store_acc_rows<D>(tmem + lane_off + BT_ACC0 + D, p.scale, p.dk, row_flat, row_ok);
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == BWD_MMA_WARP) tmem_dealloc(tmem, BWD_TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                        const BwdParams p) {
+  using C = BwdCfg<D>;
+  using M = BwdMma<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  auto bar = [&](int id) -> uint32_t { return base + C::BAR_OFF + 8u * (uint32_t)id; };
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
+
+  // unit: heaviest first (under causal the last query tiles see the most keys)
+  const int BH = p.B * p.H;
+  const int it_rev = (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / p.H;
+  const int kl = clamp_kl(p, b);
+  const int it = p.causal ? p.n_tiles - 1 - it_rev : it_rev;
+  const int q0 = it * 128;
+  const int kl_tiles = (kl + 127) / 128;
+  const int n_k = p.causal ? min(it + 1, kl_tiles) : kl_tiles;  // key tiles this query tile sees
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_FIX_FULL), 1);
+    for (int s = 0; s < BWD_STAGES; ++s) {
+      mbar_init(bar(C::B_ST_FULL + s), 1);
+      mbar_init(bar(C::B_ST_EMPTY + s), 1);
+    }
+    mbar_init(bar(C::B_S_FULL), 1);
+    mbar_init(bar(C::B_DP_FULL), 1);
+    mbar_init(bar(C::B_OPS_READY), 128);
+    mbar_init(bar(C::B_ACC_FULL), 1);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BWD_PRODUCER_WARP && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    prefetch_tensormap(&tmap_do);
+  }
+  if (warp == BWD_MMA_WARP) {
+    tmem_alloc(base + C::MISC_OFF, BWD_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_slot;
+  Waiter waiter{abort_flag, p.err, p.wait_limit_ns, 0};
+  const int u = (int)blockIdx.x;
+
+  if (n_k > 0 && warp == BWD_PRODUCER_WARP) {
+    if (lane == 0) {
+      waiter.role = ROLE_PRODUCER;
+      bool ok = true;
+      mbar_arrive_expect_tx(bar(C::B_FIX_FULL), 2 * C::TILE_BYTES);
+#pragma unroll
+      for (int pn = 0; pn < C::PANELS; ++pn) {
+        tma_load_3d(base + C::FIX0_OFF + pn * PANEL_BYTES, &tmap_q, bar(C::B_FIX_FULL), 64 * pn, q0, bh);
+        tma_load_3d(base + C::FIX1_OFF + pn * PANEL_BYTES, &tmap_do, bar(C::B_FIX_FULL), 64 * pn, q0, bh);
+      }
+      int issued = 0;
+      for (int n = 0; ok && n < n_k; ++n) {
+        const int s = n % BWD_STAGES;
+        ok = wait_bar(waiter, bar(C::B_ST_EMPTY + s), ((n / BWD_STAGES) & 1) ^ 1, C::B_ST_EMPTY + s, u);
+        if (!ok) break;
+        const uint32_t full = bar(C::B_ST_FULL + s);
+        mbar_arrive_expect_tx(full, 2 * C::TILE_BYTES);
+        const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+          tma_load_3d(st + pn * PANEL_BYTES, &tmap_k, full, 64 * pn, n * 128, bh);
+          tma_load_3d(st + C::TILE_BYTES + pn * PANEL_BYTES, &tmap_v, full, 64 * pn, n * 128, bh);
+        }
+        issued = n + 1;
+      }
+      drain_wait(bar(C::B_FIX_FULL), 0, 20000000ull);
+      for (int n = issued > BWD_STAGES ? issued - BWD_STAGES : 0; n < issued; ++n)
+        drain_wait(bar(C::B_ST_FULL + n % BWD_STAGES), (n / BWD_STAGES) & 1, 20000000ull);
+    }
+  } else if (n_k > 0 && warp == BWD_MMA_WARP) {
+    waiter.role = ROLE_MMA;
+    bool ok = wait_bar(waiter, bar(C::B_FIX_FULL), 0, C::B_FIX_FULL, u);
+    ok = __all_sync(0xffffffffu, ok);
+    bool issued_any = false;
+    const uint64_t q_desc = smem_desc(base + C::FIX0_OFF, 16, 1024);
+    const uint64_t do_desc = smem_desc(base + C::FIX1_OFF, 16, 1024);
+    for (int n = 0; ok && n < n_k; ++n) {
+      const int s = n % BWD_STAGES;
+      ok = wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      issued_any = true;
+      tc_fence_after();
+      const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
+      M::ss(tmem + BT_S, q_desc, smem_desc(st, 16, 1024));                    // S = Q K^T
+      mma_commit_w(bar(C::B_S_FULL));
+      M::ss(tmem + BT_DP, do_desc, smem_desc(st + C::TILE_BYTES, 16, 1024));  // dP = dO V^T
+      mma_commit_w(bar(C::B_DP_FULL));
+      ok = wait_bar(waiter, bar(C::B_OPS_READY), n & 1, C::B_OPS_READY, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      M::ts(tmem + BT_ACC0, tmem + BT_S, smem_desc(st, PANEL_BYTES, 1024), n > 0 ? 1u : 0u);  // dQ += dS K
+      mma_commit_w(bar(C::B_ST_EMPTY + s));
+    }
+    if (ok) mma_commit_w(bar(C::B_ACC_FULL));
+    if (issued_any) {
+      mma_commit_w(bar(C::B_DRAIN));
+      drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
+    }
+  } else if (warp < 4) {
+    waiter.role = ROLE_SOFTMAX;
+    const int r = warp * 32 + lane;  // query row within the tile = TMEM lane
+    const int query = q0 + r;
+    const size_t row_flat = (size_t)bh * (size_t)p.N + (size_t)query;
+    const bool row_ok = query < p.N;
+    if (n_k == 0) {
+      store_zero_rows<D>(p.dq, row_flat, row_ok);
+    } else {
+      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+      const uint32_t s_addr = tmem + lane_off + BT_S;
+      const uint32_t dp_addr = tmem + lane_off + BT_DP;
+      const float c = p.scale_log2;
+      const size_t prow = (size_t)bh * (size_t)p.N_pad + (size_t)query;
+      const float lse2 = p.lse2[prow];
+      const float drow = p.delta[prow];
+      // keys [0, lim) are visible to this row
+      const int lim = p.causal ? min(kl, query + 1) : kl;
+      bool ok = true;
+      for (int n = 0; ok && n < n_k; ++n) {
+        ok = wait_bar(waiter, bar(C::B_S_FULL), n & 1, C::B_S_FULL, u);
+        if (ok) ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int vis_n = lim - n * 128;  // columns [0, vis_n) visible
+        const bool masked = vis_n < 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sh[64], dh[64];
+          tmem_ld64(s_addr + 64u * h, sh);
+          tmem_ld64(dp_addr + 64u * h, dh);
+          tmem_ld_wait(sh);
+          tmem_ld_wait(dh);
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int col = 64 * h + 2 * q;
+            float p0 = ex2(fmaf(__uint_as_float(sh[2 * q]), c, -lse2));
+            float p1 = ex2(fmaf(__uint_as_float(sh[2 * q + 1]), c, -lse2));
+            if (masked) {
+              p0 = col < vis_n ? p0 : 0.0f;
+              p1 = col + 1 < vis_n ? p1 : 0.0f;
+            }
+            pk[q] = pack_bf16x2(p0 * (__uint_as_float(dh[2 * q]) - drow), p1 * (__uint_as_float(dh[2 * q + 1]) - drow));
+          }
+          tmem_st32(s_addr + 32u * h, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_OPS_READY));
+      }
+      if (ok) {
+        ok = wait_bar(waiter, bar(C::B_ACC_FULL), 0, C::B_ACC_FULL, u);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        store_acc_rows<D>(tmem + lane_off + BT_ACC0, p.scale, p.dq, row_flat, row_ok);
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == BWD_MMA_WARP) tmem_dealloc(tmem, BWD_TMEM_COLS);
+}
+
+}  // namespace fattn

@@ -88,6 +88,40 @@ typedef enum {
 FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
               int d, float scale, int causal, const int32_t* key_len, void* stream);
 
+/*
+ * fattn_bwd: gradients of a scalar loss through the forward above.
+ *
+ * What it computes ("understand-flashattention", section "Attention forward
+ * and backward formulas", backward pass steps 1-5; P recomputed from the
+ * saved logsumexp as in "recomputing P needs logsumexp"), with
+ * S = scale * Q K^T masked as in fattn_fwd and P = exp(S - LSE):
+ *     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - rowsum(dO * O)),
+ *     dQ = scale * dS K,   dK = scale * dS^T Q.
+ * (rowsum(dO * O)_i equals sum_k dP_ik P_ik, the row term of step 3.)
+ *
+ *   q, k, v  the forward's inputs, bf16 [B, H, N, d] (as for fattn_fwd).
+ *   o, lse   the forward's outputs for the same q, k, v, scale, causal and
+ *            key_len: bf16 O [B, H, N, d] and fp32 LSE [B, H, N].
+ *   dout     dL/dO, bf16 [B, H, N, d].
+ *   dq, dk, dv  written: bf16 [B, H, N, d]; each rounded once from fp32.
+ *   B, H, N, d, scale, causal, key_len, stream: as for fattn_fwd.
+ *
+ * A query row with no visible key gets dQ = 0; a key visible to no query
+ * (key_len) gets dK = dV = 0.  All device pointers 16-byte aligned (lse and
+ * key_len 4-byte); the caller owns every tensor.  Each call takes
+ * 2 * B*H*ceil(N/128)*128 * 4 bytes of scratch from the library's pool on
+ * `stream` (per-row D and LSE in base 2) and returns it in stream order;
+ * it enqueues three kernels on `stream` and returns without synchronising.
+ *
+ * Returns FATTN_OK, FATTN_ERR_INVALID_ARG, FATTN_ERR_UNSUPPORTED (d not in
+ * {64, 128}) or FATTN_ERR_CUDA, with argument errors detected before anything
+ * is enqueued; time-outs of the kernels' bounded waits are reported by
+ * fattn_last_error().
+ */
+FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                        int causal, const int32_t* key_len, void* stream);
+
 /* A static, human-readable name for a status code. */
 FATTN_API const char* fattn_status_string(int status);
 

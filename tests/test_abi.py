@@ -112,6 +112,29 @@ def test_host_pointer_rejected(lib):
     assert call(q=addr, k=addr, v=addr, o=addr, lse=addr) == binding.FATTN_ERR_INVALID_ARG
 
 
+def bcall(B=1, H=1, N=128, d=64, scale=0.125, causal=0, kl=None, **ptrs):
+    names = ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")
+    a = {n: ptrs.get(n, FAKE) for n in names}
+    return binding.bwd_raw(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], B, H, N, d,
+                           scale, causal, kl, None)
+
+
+def test_backward_argument_checks(lib):
+    assert bcall(B=0) == binding.FATTN_OK
+    assert bcall(N=-1) == binding.FATTN_ERR_INVALID_ARG
+    assert bcall(scale=math.nan) == binding.FATTN_ERR_INVALID_ARG
+    for name in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv"):
+        assert bcall(**{name: 0}) == binding.FATTN_ERR_INVALID_ARG, name
+    for name in ("q", "k", "v", "o", "dout", "dq", "dk", "dv"):
+        assert bcall(**{name: FAKE + 8}) == binding.FATTN_ERR_INVALID_ARG, name
+    assert bcall(lse=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
+    assert bcall(d=96) == binding.FATTN_ERR_UNSUPPORTED
+    buf = np.zeros(128 * 64 * 4, dtype=np.uint8)
+    addr = buf.ctypes.data + (-buf.ctypes.data) % 16
+    host = {n: addr for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")}
+    assert bcall(**host) == binding.FATTN_ERR_INVALID_ARG
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "libfattn.so"))
     monkeypatch.setattr(binding, "_lib", None)
