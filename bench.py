@@ -20,6 +20,10 @@ divided by the slowest rank's time (weak scaling).
 --impl reference times the fp64 CPU oracle (plain loops, the definition of the
 result) on the host cores, on a bounded sample of query rows of the same
 workload, in the same metric.
+
+--pass bwd times the backward instead (fattn_bwd: dQ, dK, dV from dO and the
+forward's O and LSE, which are computed once before the timed region), with
+FLOPs counted as 2.5x the forward's (five GEMMs of the forward's size).
 """
 from __future__ import annotations
 
@@ -341,6 +345,121 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     print(json.dumps(line), flush=True)
 
 
+def bwd_arm(args, rank: int, world: int, local_rank: int):
+    """The backward pass, timed like the forward (one JSON line on rank 0)."""
+    import torch
+
+    import oracle
+    from exact_softmax_attention_fattn_gb300 import binding
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    w = WORKLOADS[args.workload]
+    x = make_inputs(w)
+    g_bits = make_inputs(w.replace(seed=w.seed + 1000)).v  # dL/dO ~ N(0, 1)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v, go = dev_bf16(x.q), dev_bf16(x.k), dev_bf16(x.v), dev_bf16(g_bits)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    kl = None if x.key_len is None else torch.from_numpy(x.key_len).to(dev)
+    binding.forward_into(q, k, v, o, lse, causal=w.causal, scale=w.softmax_scale, key_len=kl)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = 2.5 * causal_flops(w, x.key_len)
+
+    def step():
+        binding.backward_into(q, k, v, o, lse, go, dq, dk, dv, causal=w.causal, scale=w.softmax_scale, key_len=kl)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    st, detail = binding.last_error(stream)
+    if st != binding.FATTN_OK:
+        raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    st, detail = binding.last_error(stream)
+    if st != binding.FATTN_OK:
+        raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
+    kernel_ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    ms_per_step, value = aggregate_ranks(float(sum(kernel_ms)), flops, args.steps, world, dev)
+
+    # end to end: the six inputs copied in from pinned host buffers, three gradients copied out
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (q, k, v, o, go)] + [lse.cpu().pin_memory()]
+        host_out = [torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+        dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+        n_e2e = max(3, min(args.steps, 10))
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            for hd, dd in zip(host_in, dev_in):
+                dd.copy_(hd, non_blocking=True)
+            binding.backward_into(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[5], dev_in[4], dq, dk, dv,
+                                  causal=w.causal, scale=w.softmax_scale, key_len=kl)
+            for hd, dd in zip(host_out, (dq, dk, dv)):
+                hd.copy_(dd, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        e2e = {"value": flops / e2e_s / 1e12 * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+    if rank != 0:
+        return
+    peak, peak_kind, _ = measured_peaks()
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        # the fp64 oracle backward on one head (about 2.5x the head's forward FLOPs)
+        t0 = time.perf_counter()
+        oracle.backward(x.q, x.k, x.v, g_bits, w.softmax_scale, w.causal, key_len=x.key_len, heads=[0])
+        dt = time.perf_counter() - t0
+        head_flops = flops / (w.B * w.H)
+        cpu = {"value": head_flops / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+               "sample": f"head 0 of {w.B * w.H} ({args.workload}), full fp64 backward", "seconds": round(dt, 2)}
+    line = {
+        "metric": "attention bwd TFLOP/s (causal-adjusted, 2.5x forward FLOPs) and % of GB300 bf16 dense peak",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded SplitMix64/Box-Muller, bf16-rounded)",
+        "config": {"workload": args.workload, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "key_padding": x.key_len is not None, "flops_per_step": flops,
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}", "traffic": None},
+        "pct_of_bf16_peak": 100.0 * achieved / peak,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,  # prep + dK/dV + dQ kernels per step
+        "kernel": "fattn_bwd_prep_kernel + fattn_bwd_dkdv_kernel + fattn_bwd_dq_kernel",
+        "kernel_ms": {"min": min(kernel_ms), "median": float(np.median(kernel_ms)), "max": max(kernel_ms)},
+        "wall_s_timed_region": wall,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -351,6 +470,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -368,7 +489,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        our_arm(args, rank, world, local_rank)
+        (bwd_arm if args.pass_ == "bwd" else our_arm)(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist
