@@ -109,10 +109,11 @@ struct BwdCfg {
   static constexpr int B_ST_EMPTY = 1 + BWD_STAGES;      // [BWD_STAGES]
   static constexpr int B_S_FULL = 1 + 2 * BWD_STAGES;
   static constexpr int B_DP_FULL = B_S_FULL + 1;
-  static constexpr int B_OPS_READY = B_S_FULL + 2;       // P^T / dS^T (or dS) stored
+  static constexpr int B_OPS_READY = B_S_FULL + 2;       // P^T stored (dK/dV kernel) or dS stored (dQ kernel)
   static constexpr int B_ACC_FULL = B_S_FULL + 3;
   static constexpr int B_DRAIN = B_S_FULL + 4;
-  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr int B_DS_READY = B_S_FULL + 5;        // dS^T stored (dK/dV kernel)
+  static constexpr int NUM_BARS = B_DS_READY + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
   // + slack for 1024-byte alignment; at least 120 KB so that only one CTA fits
   // an SM (each allocates all 512 TMEM columns)
@@ -226,6 +227,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
     mbar_init(bar(C::B_OPS_READY), 128);
+    mbar_init(bar(C::B_DS_READY), 128);
     mbar_init(bar(C::B_ACC_FULL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -283,32 +285,60 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         drain_wait(bar(C::B_ST_FULL + n % BWD_STAGES), (n / BWD_STAGES) & 1, 20000000ull);
     }
   } else if (n_q > 0 && warp == BWD_MMA_WARP) {
+    // Per query tile n the order is S(n), dP(n), dV(n), S(n+1), dK(n), dP(n+1):
+    // dV waits only for P^T, dK for dS^T, and the next tile's S^T is computed
+    // while the elementwise warps form dS^T, so that the exponentials of tile
+    // n+1 overlap dK(n) and dP(n+1).  S(n+1) may overwrite P^T(n) once dV(n)
+    // has been issued (the tensor pipe runs in order); dP(n+1) overwrites
+    // dS^T(n) after dK(n).
     waiter.role = ROLE_MMA;
     bool ok = wait_bar(waiter, bar(C::B_FIX_FULL), 0, C::B_FIX_FULL, u);
     ok = __all_sync(0xffffffffu, ok);
     bool issued_any = false;
     const uint64_t k_desc = smem_desc(base + C::FIX0_OFF, 16, 1024);
     const uint64_t v_desc = smem_desc(base + C::FIX1_OFF, 16, 1024);
-    for (int n = 0; ok && n < n_q; ++n) {
+    auto stage_addr = [&](int n) { return base + C::RING_OFF + (uint32_t)(n % BWD_STAGES) * C::STAGE_BYTES; };
+    auto wait_stage = [&](int n) {
       const int s = n % BWD_STAGES;
-      ok = wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
+      ok = ok && wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+    };
+    auto issue_s = [&](int n) {  // S^T = K Q^T
+      M::ss(tmem + BT_S, k_desc, smem_desc(stage_addr(n), 16, 1024));
+      mma_commit_w(bar(C::B_S_FULL));
+    };
+    auto issue_dp = [&](int n) {  // dP^T = V dO^T
+      M::ss(tmem + BT_DP, v_desc, smem_desc(stage_addr(n) + C::TILE_BYTES, 16, 1024));
+      mma_commit_w(bar(C::B_DP_FULL));
+    };
+    wait_stage(0);
+    if (ok) {
       issued_any = true;
       tc_fence_after();
-      const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
-      M::ss(tmem + BT_S, k_desc, smem_desc(st, 16, 1024));                  // S^T = K Q^T
-      mma_commit_w(bar(C::B_S_FULL));
-      M::ss(tmem + BT_DP, v_desc, smem_desc(st + C::TILE_BYTES, 16, 1024));  // dP^T = V dO^T
-      mma_commit_w(bar(C::B_DP_FULL));
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int n = 0; ok && n < n_q; ++n) {
+      const uint32_t st = stage_addr(n);
+      const uint32_t acc = n > 0 ? 1u : 0u;
       ok = wait_bar(waiter, bar(C::B_OPS_READY), n & 1, C::B_OPS_READY, u);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t acc = n > 0 ? 1u : 0u;
       M::ts(tmem + BT_ACC0, tmem + BT_S, smem_desc(st + C::TILE_BYTES, PANEL_BYTES, 1024), acc);  // dV += P^T dO
-      M::ts(tmem + BT_ACC0 + D, tmem + BT_DP, smem_desc(st, PANEL_BYTES, 1024), acc);          // dK += dS^T Q
-      mma_commit_w(bar(C::B_ST_EMPTY + s));
+      if (n + 1 < n_q) {
+        wait_stage(n + 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(n + 1);
+      }
+      ok = wait_bar(waiter, bar(C::B_DS_READY), n & 1, C::B_DS_READY, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      M::ts(tmem + BT_ACC0 + D, tmem + BT_DP, smem_desc(st, PANEL_BYTES, 1024), acc);  // dK += dS^T Q
+      mma_commit_w(bar(C::B_ST_EMPTY + n % BWD_STAGES));
+      if (n + 1 < n_q) issue_dp(n + 1);
     }
     if (ok) mma_commit_w(bar(C::B_ACC_FULL));
     if (issued_any) {
@@ -336,7 +366,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const int q0 = (i_first + n) * 128;
         ok = wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
         if (ok) ok = wait_bar(waiter, bar(C::B_S_FULL), n & 1, C::B_S_FULL, u);
-        if (ok) ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -347,40 +376,59 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // contribute nothing (their dO and Q are zero)
         const int min_q = p.causal ? key - q0 : 0;  // columns < min_q are masked
         const bool any_mask = !key_vis || min_q > 0;
+        // phase 1: P^T (kept in fp32 for dS^T), released for dV as soon as it is stored
+        float pr[128];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t sh[64], dh[64];
+          uint32_t sh[64];
           tmem_ld64(s_addr + 64u * h, sh);
-          tmem_ld64(dp_addr + 64u * h, dh);
           tmem_ld_wait(sh);
-          tmem_ld_wait(dh);
-          uint32_t pk[32], dk2[32];
+          uint32_t pk[32];
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 l4 = lse4[16 * h + q4];
-            const float4 d4 = del4[16 * h + q4];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int col = 64 * h + 4 * q4 + e;
               float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
               if (any_mask) pe = (key_vis && col >= min_q) ? pe : 0.0f;
-              pv[e] = pe;
-              dsv[e] = pe * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
+              pr[col] = pe;
             }
-            pk[2 * q4] = pack_bf16x2(pv[0], pv[1]);
-            pk[2 * q4 + 1] = pack_bf16x2(pv[2], pv[3]);
-            dk2[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-            dk2[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+            pk[2 * q4] = pack_bf16x2(pr[64 * h + 4 * q4], pr[64 * h + 4 * q4 + 1]);
+            pk[2 * q4 + 1] = pack_bf16x2(pr[64 * h + 4 * q4 + 2], pr[64 * h + 4 * q4 + 3]);
           }
           tmem_st32(s_addr + 32u * h, pk);
-          tmem_st32(dp_addr + 32u * h, dk2);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::B_OPS_READY));
+        // phase 2: dS^T = P^T (dP^T - D)
+        ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t dh[64];
+          tmem_ld64(dp_addr + 64u * h, dh);
+          tmem_ld_wait(dh);
+          uint32_t dk2[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            const float4 d4 = del4[16 * h + q4];
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dsv[e] = pr[64 * h + 4 * q4 + e] * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
+            dk2[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
+            dk2[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+          }
+          tmem_st32(dp_addr + 32u * h, dk2);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DS_READY));
       }
       if (ok) {
         ok = wait_bar(waiter, bar(C::B_ACC_FULL), 0, C::B_ACC_FULL, u);
