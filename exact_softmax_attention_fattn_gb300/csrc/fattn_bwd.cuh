@@ -590,31 +590,40 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       bool ok = true;
       for (int n = 0; ok && n < n_k; ++n) {
         ok = wait_bar(waiter, bar(C::B_S_FULL), n & 1, C::B_S_FULL, u);
-        if (ok) ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         const int vis_n = lim - n * 128;  // columns [0, vis_n) visible
         const bool masked = vis_n < 128;
+        // phase 1 (while dP is computed): P in fp32 registers
+        float pr[128];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t sh[64], dh[64];
+          uint32_t sh[64];
           tmem_ld64(s_addr + 64u * h, sh);
-          tmem_ld64(dp_addr + 64u * h, dh);
           tmem_ld_wait(sh);
+#pragma unroll
+          for (int q = 0; q < 64; ++q) {
+            float pe = ex2(fmaf(__uint_as_float(sh[q]), c, -lse2));
+            if (masked) pe = 64 * h + q < vis_n ? pe : 0.0f;
+            pr[64 * h + q] = pe;
+          }
+        }
+        // phase 2: dS = P (dP - D), stored as bf16 over the first 64 columns of S
+        ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t dh[64];
+          tmem_ld64(dp_addr + 64u * h, dh);
           tmem_ld_wait(dh);
           uint32_t pk[32];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int col = 64 * h + 2 * q;
-            float p0 = ex2(fmaf(__uint_as_float(sh[2 * q]), c, -lse2));
-            float p1 = ex2(fmaf(__uint_as_float(sh[2 * q + 1]), c, -lse2));
-            if (masked) {
-              p0 = col < vis_n ? p0 : 0.0f;
-              p1 = col + 1 < vis_n ? p1 : 0.0f;
-            }
-            pk[q] = pack_bf16x2(p0 * (__uint_as_float(dh[2 * q]) - drow), p1 * (__uint_as_float(dh[2 * q + 1]) - drow));
-          }
+          for (int q = 0; q < 32; ++q)
+            pk[q] = pack_bf16x2(pr[64 * h + 2 * q] * (__uint_as_float(dh[2 * q]) - drow),
+                                pr[64 * h + 2 * q + 1] * (__uint_as_float(dh[2 * q + 1]) - drow));
           tmem_st32(s_addr + 32u * h, pk);
         }
         tmem_st_wait();
