@@ -66,7 +66,7 @@ int configure_kernel() {
   if (cudaFuncSetAttribute(fattn::fattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)fattn::BwdCfg<D>::SMEM_BYTES) != cudaSuccess ||
       cudaFuncSetAttribute(fattn::fattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)fattn::BwdCfg<D>::SMEM_BYTES) != cudaSuccess)
+                           (int)fattn::BwdDqCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FATTN_ERR_CUDA;
   return FATTN_OK;
 }
@@ -269,7 +269,8 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
   fattn::fattn_bwd_dkdv_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo,
                                                                                                       p);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  fattn::fattn_bwd_dq_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  fattn::fattn_bwd_dq_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdDqCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv,
+                                                                                                      mdo, p);
   return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 

@@ -450,12 +450,44 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ dQ
+// Q_i and dO_i stay; K_j streams through a 3-slot ring and V_j through a
+// 2-slot ring.  S is double-buffered in tensor memory (S_j in buffer j % 2):
+// per key tile the issuer runs dQ(j), dP(j+1), S(j+2), so S of the next tile
+// is long done when its exponentials start, and the K tile of S(j+2) was
+// loaded while tile j was in flight (its slot freed by dQ(j-1)).
+template <int D>
+struct BwdDqCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t TILE_BYTES = 128u * D * 2u;
+  static constexpr int K_SLOTS = 3, V_SLOTS = 2;
+  static constexpr uint32_t Q_OFF = 0, DO_OFF = TILE_BYTES;
+  static constexpr uint32_t K_OFF = 2 * TILE_BYTES;
+  static constexpr uint32_t V_OFF = K_OFF + K_SLOTS * TILE_BYTES;
+  static constexpr uint32_t BAR_OFF = V_OFF + V_SLOTS * TILE_BYTES;
+  static constexpr int B_FIX_FULL = 0;
+  static constexpr int B_K_FULL = 1;                     // [K_SLOTS]
+  static constexpr int B_K_EMPTY = B_K_FULL + K_SLOTS;   // [K_SLOTS]
+  static constexpr int B_V_FULL = B_K_EMPTY + K_SLOTS;   // [V_SLOTS]
+  static constexpr int B_V_EMPTY = B_V_FULL + V_SLOTS;   // [V_SLOTS]
+  static constexpr int B_S_FULL = B_V_EMPTY + V_SLOTS;
+  static constexpr int B_DP_FULL = B_S_FULL + 1;
+  static constexpr int B_DS_READY = B_S_FULL + 2;
+  static constexpr int B_ACC_FULL = B_S_FULL + 3;
+  static constexpr int B_DRAIN = B_S_FULL + 4;
+  static constexpr int NUM_BARS = B_DRAIN + 1;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_USED = MISC_OFF + 16 + 1024;
+  static constexpr uint32_t SMEM_BYTES = SMEM_USED > 120u * 1024u ? SMEM_USED : 120u * 1024u;
+  static_assert(SMEM_USED <= 232448u, "shared memory");
+};
+constexpr uint32_t BQ_S0 = 0, BQ_DP = 256, BQ_DQ = 384;  // TMEM columns: S buffers at 0 and 128
+
 template <int D>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     fattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
                         const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdDqCfg<D>;
   using M = BwdMma<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -480,13 +512,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_FIX_FULL), 1);
-    for (int s = 0; s < BWD_STAGES; ++s) {
-      mbar_init(bar(C::B_ST_FULL + s), 1);
-      mbar_init(bar(C::B_ST_EMPTY + s), 1);
+    for (int s = 0; s < C::K_SLOTS; ++s) {
+      mbar_init(bar(C::B_K_FULL + s), 1);
+      mbar_init(bar(C::B_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < C::V_SLOTS; ++s) {
+      mbar_init(bar(C::B_V_FULL + s), 1);
+      mbar_init(bar(C::B_V_EMPTY + s), 1);
     }
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
-    mbar_init(bar(C::B_OPS_READY), 128);
+    mbar_init(bar(C::B_DS_READY), 128);
     mbar_init(bar(C::B_ACC_FULL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -516,53 +552,94 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_arrive_expect_tx(bar(C::B_FIX_FULL), 2 * C::TILE_BYTES);
 #pragma unroll
       for (int pn = 0; pn < C::PANELS; ++pn) {
-        tma_load_3d(base + C::FIX0_OFF + pn * PANEL_BYTES, &tmap_q, bar(C::B_FIX_FULL), 64 * pn, q0, bh);
-        tma_load_3d(base + C::FIX1_OFF + pn * PANEL_BYTES, &tmap_do, bar(C::B_FIX_FULL), 64 * pn, q0, bh);
+        tma_load_3d(base + C::Q_OFF + pn * PANEL_BYTES, &tmap_q, bar(C::B_FIX_FULL), 64 * pn, q0, bh);
+        tma_load_3d(base + C::DO_OFF + pn * PANEL_BYTES, &tmap_do, bar(C::B_FIX_FULL), 64 * pn, q0, bh);
       }
       int issued = 0;
       for (int n = 0; ok && n < n_k; ++n) {
-        const int s = n % BWD_STAGES;
-        ok = wait_bar(waiter, bar(C::B_ST_EMPTY + s), ((n / BWD_STAGES) & 1) ^ 1, C::B_ST_EMPTY + s, u);
+        const int ks = n % C::K_SLOTS, vs = n % C::V_SLOTS;
+        ok = wait_bar(waiter, bar(C::B_K_EMPTY + ks), ((n / C::K_SLOTS) & 1) ^ 1, C::B_K_EMPTY + ks, u);
         if (!ok) break;
-        const uint32_t full = bar(C::B_ST_FULL + s);
-        mbar_arrive_expect_tx(full, 2 * C::TILE_BYTES);
-        const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(bar(C::B_K_FULL + ks), C::TILE_BYTES);
 #pragma unroll
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_3d(st + pn * PANEL_BYTES, &tmap_k, full, 64 * pn, n * 128, bh);
-          tma_load_3d(st + C::TILE_BYTES + pn * PANEL_BYTES, &tmap_v, full, 64 * pn, n * 128, bh);
-        }
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_3d(base + C::K_OFF + (uint32_t)ks * C::TILE_BYTES + pn * PANEL_BYTES, &tmap_k, bar(C::B_K_FULL + ks),
+                      64 * pn, n * 128, bh);
+        ok = wait_bar(waiter, bar(C::B_V_EMPTY + vs), ((n / C::V_SLOTS) & 1) ^ 1, C::B_V_EMPTY + vs, u);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(C::B_V_FULL + vs), C::TILE_BYTES);
+#pragma unroll
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_3d(base + C::V_OFF + (uint32_t)vs * C::TILE_BYTES + pn * PANEL_BYTES, &tmap_v, bar(C::B_V_FULL + vs),
+                      64 * pn, n * 128, bh);
         issued = n + 1;
       }
       drain_wait(bar(C::B_FIX_FULL), 0, 20000000ull);
-      for (int n = issued > BWD_STAGES ? issued - BWD_STAGES : 0; n < issued; ++n)
-        drain_wait(bar(C::B_ST_FULL + n % BWD_STAGES), (n / BWD_STAGES) & 1, 20000000ull);
+      for (int n = issued > C::V_SLOTS ? issued - C::V_SLOTS : 0; n < issued; ++n)
+        drain_wait(bar(C::B_V_FULL + n % C::V_SLOTS), (n / C::V_SLOTS) & 1, 20000000ull);
+      for (int n = issued > C::K_SLOTS ? issued - C::K_SLOTS : 0; n < issued; ++n)
+        drain_wait(bar(C::B_K_FULL + n % C::K_SLOTS), (n / C::K_SLOTS) & 1, 20000000ull);
     }
   } else if (n_k > 0 && warp == BWD_MMA_WARP) {
     waiter.role = ROLE_MMA;
     bool ok = wait_bar(waiter, bar(C::B_FIX_FULL), 0, C::B_FIX_FULL, u);
     ok = __all_sync(0xffffffffu, ok);
     bool issued_any = false;
-    const uint64_t q_desc = smem_desc(base + C::FIX0_OFF, 16, 1024);
-    const uint64_t do_desc = smem_desc(base + C::FIX1_OFF, 16, 1024);
-    for (int n = 0; ok && n < n_k; ++n) {
-      const int s = n % BWD_STAGES;
-      ok = wait_bar(waiter, bar(C::B_ST_FULL + s), (n / BWD_STAGES) & 1, C::B_ST_FULL + s, u);
+    const uint64_t q_desc = smem_desc(base + C::Q_OFF, 16, 1024);
+    const uint64_t do_desc = smem_desc(base + C::DO_OFF, 16, 1024);
+    auto k_addr = [&](int n) { return base + C::K_OFF + (uint32_t)(n % C::K_SLOTS) * C::TILE_BYTES; };
+    auto v_addr = [&](int n) { return base + C::V_OFF + (uint32_t)(n % C::V_SLOTS) * C::TILE_BYTES; };
+    auto wait_k = [&](int n) {
+      const int s = n % C::K_SLOTS;
+      ok = ok && wait_bar(waiter, bar(C::B_K_FULL + s), (n / C::K_SLOTS) & 1, C::B_K_FULL + s, u);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      issued_any = true;
+    };
+    auto wait_v = [&](int n) {
+      const int s = n % C::V_SLOTS;
+      ok = ok && wait_bar(waiter, bar(C::B_V_FULL + s), (n / C::V_SLOTS) & 1, C::B_V_FULL + s, u);
+      ok = __all_sync(0xffffffffu, ok);
+    };
+    auto issue_s = [&](int n) {  // S_n = Q K_n^T into buffer n % 2
       tc_fence_after();
-      const uint32_t st = base + C::RING_OFF + (uint32_t)s * C::STAGE_BYTES;
-      M::ss(tmem + BT_S, q_desc, smem_desc(st, 16, 1024));                    // S = Q K^T
+      M::ss(tmem + BQ_S0 + 128u * (uint32_t)(n & 1), q_desc, smem_desc(k_addr(n), 16, 1024));
       mma_commit_w(bar(C::B_S_FULL));
-      M::ss(tmem + BT_DP, do_desc, smem_desc(st + C::TILE_BYTES, 16, 1024));  // dP = dO V^T
+    };
+    auto issue_dp = [&](int n) {  // dP_n = dO V_n^T; V_n is then free
+      tc_fence_after();
+      M::ss(tmem + BQ_DP, do_desc, smem_desc(v_addr(n), 16, 1024));
       mma_commit_w(bar(C::B_DP_FULL));
-      ok = wait_bar(waiter, bar(C::B_OPS_READY), n & 1, C::B_OPS_READY, u);
+      mma_commit_w(bar(C::B_V_EMPTY + n % C::V_SLOTS));
+    };
+    if (ok) {
+      issued_any = true;
+      wait_k(0);
+      if (ok) issue_s(0);
+      wait_v(0);
+      if (ok) issue_dp(0);
+      if (n_k > 1) {
+        wait_k(1);
+        if (ok) issue_s(1);
+      }
+    }
+    for (int n = 0; ok && n < n_k; ++n) {
+      ok = wait_bar(waiter, bar(C::B_DS_READY), n & 1, C::B_DS_READY, u);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      M::ts(tmem + BT_ACC0, tmem + BT_S, smem_desc(st, PANEL_BYTES, 1024), n > 0 ? 1u : 0u);  // dQ += dS K
-      mma_commit_w(bar(C::B_ST_EMPTY + s));
+      // dQ += dS_n K_n (dS over the first 64 columns of S buffer n % 2); K_n is then free
+      M::ts(tmem + BQ_DQ, tmem + BQ_S0 + 128u * (uint32_t)(n & 1), smem_desc(k_addr(n), PANEL_BYTES, 1024),
+            n > 0 ? 1u : 0u);
+      mma_commit_w(bar(C::B_K_EMPTY + n % C::K_SLOTS));
+      if (n + 1 < n_k) {
+        wait_v(n + 1);
+        if (!ok) break;
+        issue_dp(n + 1);
+      }
+      if (n + 2 < n_k) {
+        wait_k(n + 2);
+        if (!ok) break;
+        issue_s(n + 2);
+      }
     }
     if (ok) mma_commit_w(bar(C::B_ACC_FULL));
     if (issued_any) {
@@ -579,8 +656,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       store_zero_rows<D>(p.dq, row_flat, row_ok);
     } else {
       const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-      const uint32_t s_addr = tmem + lane_off + BT_S;
-      const uint32_t dp_addr = tmem + lane_off + BT_DP;
+      const uint32_t dp_addr = tmem + lane_off + BQ_DP;
       const float c = p.scale_log2;
       const size_t prow = (size_t)bh * (size_t)p.N_pad + (size_t)query;
       const float lse2 = p.lse2[prow];
@@ -589,6 +665,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int lim = p.causal ? min(kl, query + 1) : kl;
       bool ok = true;
       for (int n = 0; ok && n < n_k; ++n) {
+        const uint32_t s_addr = tmem + lane_off + BQ_S0 + 128u * (uint32_t)(n & 1);
         ok = wait_bar(waiter, bar(C::B_S_FULL), n & 1, C::B_S_FULL, u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -628,7 +705,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::B_OPS_READY));
+        mbar_arrive(bar(C::B_DS_READY));
       }
       if (ok) {
         ok = wait_bar(waiter, bar(C::B_ACC_FULL), 0, C::B_ACC_FULL, u);
@@ -636,7 +713,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        store_acc_rows<D>(tmem + lane_off + BT_ACC0, p.scale, p.dq, row_flat, row_ok);
+        store_acc_rows<D>(tmem + lane_off + BQ_DQ, p.scale, p.dq, row_flat, row_ok);
       }
     }
   }
