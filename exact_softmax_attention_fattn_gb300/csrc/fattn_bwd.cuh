@@ -469,11 +469,14 @@ struct BwdDqCfg {
   static constexpr int B_K_EMPTY = B_K_FULL + K_SLOTS;   // [K_SLOTS]
   static constexpr int B_V_FULL = B_K_EMPTY + K_SLOTS;   // [V_SLOTS]
   static constexpr int B_V_EMPTY = B_V_FULL + V_SLOTS;   // [V_SLOTS]
-  static constexpr int B_S_FULL = B_V_EMPTY + V_SLOTS;
-  static constexpr int B_DP_FULL = B_S_FULL + 1;
-  static constexpr int B_DS_READY = B_S_FULL + 2;
-  static constexpr int B_ACC_FULL = B_S_FULL + 3;
-  static constexpr int B_DRAIN = B_S_FULL + 4;
+  // one S barrier per tensor-memory S buffer: S(0) and S(1) are issued back
+  // to back, so a shared barrier could complete both phases before the
+  // elementwise warps first look at it, and a parity wait would then miss
+  static constexpr int B_S_FULL = B_V_EMPTY + V_SLOTS;  // [2]
+  static constexpr int B_DP_FULL = B_S_FULL + 2;
+  static constexpr int B_DS_READY = B_S_FULL + 3;
+  static constexpr int B_ACC_FULL = B_S_FULL + 4;
+  static constexpr int B_DRAIN = B_S_FULL + 5;
   static constexpr int NUM_BARS = B_DRAIN + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16 + 1024;
@@ -521,6 +524,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(bar(C::B_V_EMPTY + s), 1);
     }
     mbar_init(bar(C::B_S_FULL), 1);
+    mbar_init(bar(C::B_S_FULL + 1), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
     mbar_init(bar(C::B_DS_READY), 128);
     mbar_init(bar(C::B_ACC_FULL), 1);
@@ -602,7 +606,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     auto issue_s = [&](int n) {  // S_n = Q K_n^T into buffer n % 2
       tc_fence_after();
       M::ss(tmem + BQ_S0 + 128u * (uint32_t)(n & 1), q_desc, smem_desc(k_addr(n), 16, 1024));
-      mma_commit_w(bar(C::B_S_FULL));
+      mma_commit_w(bar(C::B_S_FULL + (n & 1)));
     };
     auto issue_dp = [&](int n) {  // dP_n = dO V_n^T; V_n is then free
       tc_fence_after();
@@ -666,7 +670,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       bool ok = true;
       for (int n = 0; ok && n < n_k; ++n) {
         const uint32_t s_addr = tmem + lane_off + BQ_S0 + 128u * (uint32_t)(n & 1);
-        ok = wait_bar(waiter, bar(C::B_S_FULL), n & 1, C::B_S_FULL, u);
+        ok = wait_bar(waiter, bar(C::B_S_FULL + (n & 1)), (n >> 1) & 1, C::B_S_FULL + (n & 1), u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
