@@ -22,7 +22,8 @@ FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
-EXPORTED = ("fattn_fwd", "fattn_bwd", "fattn_status_string", "fattn_last_error", "fattn_version")
+EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_splitkv_plan", "fattn_bwd", "fattn_status_string",
+            "fattn_last_error", "fattn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +60,14 @@ def load_library():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_void_p,
             ]
+            lib.fattn_fwd_splitkv.restype = ctypes.c_int
+            lib.fattn_fwd_splitkv.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+            ]
+            lib.fattn_splitkv_plan.restype = ctypes.c_int
+            lib.fattn_splitkv_plan.argtypes = [ctypes.c_int] * 6
             lib.fattn_bwd.restype = ctypes.c_int
             lib.fattn_bwd.argtypes = [ctypes.c_void_p] * 9 + [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
@@ -79,10 +88,19 @@ def status_string(status: int) -> str:
 
 
 def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, d: int,
-            scale: float, causal: bool, key_len_ptr: int | None, stream: int | None) -> int:
-    """fattn_fwd with raw addresses; returns the status code."""
-    return load_library().fattn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
-                                    float(scale), int(bool(causal)), key_len_ptr, stream)
+            scale: float, causal: bool, key_len_ptr: int | None, stream: int | None, n_splits: int | None = None) -> int:
+    """fattn_fwd (n_splits None) or fattn_fwd_splitkv with raw addresses; returns the status code."""
+    if n_splits is None:
+        return load_library().fattn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
+                                        float(scale), int(bool(causal)), key_len_ptr, stream)
+    return load_library().fattn_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
+                                            float(scale), int(bool(causal)), key_len_ptr, int(n_splits), stream)
+
+
+def splitkv_plan(B: int, H: int, N: int, causal: bool, num_sms: int, n_splits: int = 0) -> int:
+    """fattn_splitkv_plan: key splits per query block the forward uses; host only."""
+    return load_library().fattn_splitkv_plan(int(B), int(H), int(N), int(bool(causal)), int(num_sms),
+                                             int(n_splits))
 
 
 def bwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, do_ptr: int, lse_ptr: int, dq_ptr: int, dk_ptr: int,
@@ -121,9 +139,11 @@ def _check_qkv(q, k, v):
 
 
 def forward_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None, key_len=None,
-                 stream=None) -> None:
+                 stream=None, n_splits: int | None = None) -> None:
     """Run the kernel on device tensors, writing `o` (bf16 [B,H,N,d]) and `lse`
-    (fp32 [B,H,N]) in place; enqueued on `stream` (default: current stream)."""
+    (fp32 [B,H,N]) in place; enqueued on `stream` (default: current stream).
+    n_splits: None (fattn_fwd, the library's split-KV choice) or a split count
+    for fattn_fwd_splitkv (0 = the library's choice, 1 = no split)."""
     import torch
 
     _check_qkv(q, k, v)
@@ -142,9 +162,9 @@ def forward_into(q, k, v, o, lse, causal: bool = False, scale: float | None = No
     with torch.cuda.device(q.device):
         handle = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
         st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
-                     causal, kl_ptr, handle)
+                     causal, kl_ptr, handle, n_splits)
     if st != FATTN_OK:
-        raise FattnError(st, "fattn_fwd")
+        raise FattnError(st, "fattn_fwd" if n_splits is None else "fattn_fwd_splitkv")
 
 
 def backward_into(q, k, v, o, lse, dout, dq, dk, dv, causal: bool = False, scale: float | None = None,
@@ -184,7 +204,7 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     return dq, dk, dv
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=None):
+def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=None, n_splits: int | None = None):
     """O, LSE = attention forward of bf16 [B, H, N, d] tensors.
 
     Device tensors: the kernel is enqueued on the current stream and the call
@@ -212,7 +232,7 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=N
     B, H, N, _ = qd.shape
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    forward_into(qd, kd, vd, o, lse, causal=causal, scale=scale, key_len=kl)
+    forward_into(qd, kd, vd, o, lse, causal=causal, scale=scale, key_len=kl, n_splits=n_splits)
     if on_host:
         o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)

@@ -4,14 +4,17 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fattn.h"
 #include "fattn_bwd.cuh"
 #include "fattn_kernel.cuh"
+#include "splitkv_combine.cuh"
 #include "v_prepass.cuh"
 
 namespace {
@@ -55,14 +58,22 @@ unsigned long long wait_limit_ns() {
 // Sets the kernel's shared-memory limit and checks that it was compiled with
 // the register count its setmaxnreg split assumes (a split larger than the
 // launch allocation would never be granted).
-template <int D>
-int configure_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(fattn::fattn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int D, bool SPLIT>
+int configure_fwd_kernel() {
+  cudaError_t e = cudaFuncSetAttribute(fattn::fattn_fwd_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)fattn::Cfg<D>::SMEM_BYTES);
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
   cudaFuncAttributes a;
-  if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D>) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D, SPLIT>) != cudaSuccess) return FATTN_ERR_CUDA;
   if (a.numRegs != fattn::LAUNCH_REGS) return FATTN_ERR_UNSUPPORTED;
+  return FATTN_OK;
+}
+
+template <int D>
+int configure_kernel() {
+  int rc = configure_fwd_kernel<D, false>();
+  if (rc == FATTN_OK) rc = configure_fwd_kernel<D, true>();
+  if (rc != FATTN_OK) return rc;
   if (cudaFuncSetAttribute(fattn::fattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)fattn::BwdCfg<D>::SMEM_BYTES) != cudaSuccess ||
       cudaFuncSetAttribute(fattn::fattn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -141,13 +152,76 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Scratch of one call: V in its per-tile storage type, then one mode byte per
-// tile, each head's row of modes padded to a multiple of 8 bytes.
-size_t scratch_bytes(int BH, int N, int D, int n_tiles) {
-  return round_up((size_t)BH * (size_t)N * (size_t)D * 2u, 256) +
-         round_up((size_t)BH * round_up((size_t)n_tiles, 8), 256);
+// tile, each head's row of modes padded to a multiple of 8 bytes; with
+// split-KV, then the fp32 partial outputs and log-sum-exps of every split.
+size_t scratch_bytes(int BH, int N, int D, int n_tiles, int n_splits = 1) {
+  size_t b = round_up((size_t)BH * (size_t)N * (size_t)D * 2u, 256) +
+             round_up((size_t)BH * round_up((size_t)n_tiles, 8), 256);
+  if (n_splits > 1)
+    b += round_up((size_t)n_splits * BH * (size_t)N * (size_t)D * 4u, 256) +
+         round_up((size_t)n_splits * BH * (size_t)N * 4u, 256);
+  return b;
 }
 
-// Enqueues the V pre-pass and the attention kernel; `scratch` must hold scratch_bytes().
+// ------------------------------------------------------------------ split-KV plan
+// Per work unit with work, a fixed cost (Q load, first S, epilogue) and, for
+// a split launch, the combine pass, both in K/V steps of the attention kernel;
+// set from GB300 timings of the low-occupancy shapes.
+constexpr double kUnitOverheadSteps = 10.0;
+constexpr double kCombineSteps = 6.0;
+constexpr int kMaxSplits = 16;
+
+// Makespan estimate, in K/V steps, of the kernel's static snake schedule for
+// one split count (key padding unknown on the host: all N keys assumed).
+// Split s of a block with n key tiles takes [s*n/splits, (s+1)*n/splits).
+double split_cost(int B, int H, int N, int causal, int num_sms, int splits) {
+  const long long BH = (long long)B * H;
+  const int nqb = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
+  const long long units = BH * nqb * splits;
+  const int G = (int)std::min<long long>(units, num_sms);
+  std::vector<double> load((size_t)G, 0.0);
+  for (long long u = 0; u < units; ++u) {
+    const long long r = u / G, i = u % G;
+    const int c = (int)((r & 1) ? G - 1 - i : i);
+    const int round = (int)(u / (BH * splits));
+    const int sp = (int)((u / BH) % splits);
+    const int r0 = (nqb - 1 - round) * fattn::QT * fattn::BM;
+    int n_blk = 0;
+    for (int t = 0; t < fattn::QT; ++t) {
+      const int row0 = r0 + t * fattn::BM;
+      if (row0 >= N) continue;
+      const int max_lim = causal ? std::min(N, row0 + fattn::BM) : N;
+      n_blk = std::max(n_blk, (max_lim + fattn::BN - 1) / fattn::BN);
+    }
+    const int n = (sp + 1) * n_blk / splits - sp * n_blk / splits;
+    if (n > 0) load[(size_t)c] += n + kUnitOverheadSteps;
+  }
+  return *std::max_element(load.begin(), load.end()) + (splits > 1 ? kCombineSteps : 0.0);
+}
+
+// K/V splits per query block.  requested > 0: that many, at most one per key
+// tile; 0: the cheapest by split_cost, searched only when the query blocks
+// alone leave SMs idle.
+int plan_splits(int B, int H, int N, int causal, int num_sms, int requested) {
+  const int n_kv = (N + fattn::BN - 1) / fattn::BN;
+  const long long units = (long long)B * H * ((N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM));
+  if (requested > 0) return std::min(requested, n_kv);
+  int best = 1;
+  if (units < num_sms && n_kv >= 2) {
+    double best_cost = split_cost(B, H, N, causal, num_sms, 1);
+    for (int sp = 2; sp <= std::min(n_kv, kMaxSplits); ++sp) {
+      const double cst = split_cost(B, H, N, causal, num_sms, sp);
+      if (cst < best_cost) {
+        best_cost = cst;
+        best = sp;
+      }
+    }
+  }
+  return best;
+}
+
+// Enqueues the V pre-pass, the attention kernel and, with split-KV, the
+// combine kernel; `scratch` must hold scratch_bytes(..., p.n_splits).
 template <int D>
 int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* scratch, int grid,
             cudaStream_t stream) {
@@ -155,6 +229,11 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
   uint8_t* v16 = reinterpret_cast<uint8_t*>(scratch);
   uint8_t* modes = v16 + round_up((size_t)BH * (size_t)p.N * D * 2u, 256);
   p.v_mode = modes;
+  if (p.n_splits > 1) {
+    uint8_t* part = modes + round_up((size_t)BH * round_up((size_t)p.n_kv_tiles, 8), 256);
+    p.o_part = reinterpret_cast<float*>(part);
+    p.lse_part = reinterpret_cast<float*>(part + round_up((size_t)p.n_splits * BH * (size_t)p.N * D * 4u, 256));
+  }
   CUtensorMap mq, mk, mv;
   if (encode_map(&mq, q, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
       encode_map(&mk, k, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
@@ -164,8 +243,20 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
   fattn::fattn_v_prepass_kernel<D><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
       reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.n_kv_tiles, p.mode_stride);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  fattn::fattn_fwd_kernel<D><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  if (p.n_splits > 1)
+    fattn::fattn_fwd_kernel<D, true><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  else
+    fattn::fattn_fwd_kernel<D, false><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  if (p.n_splits > 1) {
+    constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 4);
+    const long long n_rows = (long long)BH * p.N;
+    fattn::fattn_splitkv_combine_kernel<D>
+        <<<(unsigned)((n_rows + rows_per_block - 1) / rows_per_block), fattn::COMBINE_THREADS, 0, stream>>>(
+            p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.causal, p.n_splits);
+    if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  }
+  return FATTN_OK;
 }
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -185,10 +276,12 @@ extern "C" FATTN_API const char* fattn_status_string(int status) {
   }
 }
 
-extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                         int d, float scale, int causal, const int32_t* key_len, void* stream) {
+namespace {
+
+int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, int causal, const int32_t* key_len, int splits_requested, void* stream) {
   // ---- synchronous argument checks: nothing is enqueued on failure
-  if (B < 0 || H < 0 || N < 0) return FATTN_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || splits_requested < 0) return FATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
@@ -219,10 +312,13 @@ extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, 
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.causal = causal ? 1 : 0;
   p.n_qblocks = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
-  const long long units = (long long)B * H * p.n_qblocks;
+  p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
+  p.n_splits = plan_splits(B, H, N, p.causal, ds->num_sms, splits_requested);
+  const long long units = (long long)B * H * p.n_qblocks * p.n_splits;
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
-  p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
   p.mode_stride = (p.n_kv_tiles + 7) / 8 * 8;
   if ((long long)B * H * p.mode_stride > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.v_mode = nullptr;
@@ -231,13 +327,32 @@ extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   void* scratch = nullptr;
-  if (cudaMallocFromPoolAsync(&scratch, scratch_bytes(B * H, N, d, p.n_kv_tiles), ds->pool, s) != cudaSuccess) {
+  if (cudaMallocFromPoolAsync(&scratch, scratch_bytes(B * H, N, d, p.n_kv_tiles, p.n_splits), ds->pool, s) !=
+      cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_CUDA;
   }
   rc = d == 64 ? enqueue<64>(q, k, v, p, scratch, grid, s) : enqueue<128>(q, k, v, p, scratch, grid, s);
   if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
+}
+
+}  // namespace
+
+extern "C" FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                         int d, float scale, int causal, const int32_t* key_len, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, key_len, 0, stream);
+}
+
+extern "C" FATTN_API int fattn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                           int H, int N, int d, float scale, int causal, const int32_t* key_len,
+                                           int n_splits, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, key_len, n_splits, stream);
+}
+
+extern "C" FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits) {
+  if (B <= 0 || H <= 0 || N <= 0 || num_sms <= 0 || n_splits < 0) return 0;
+  return plan_splits(B, H, N, causal ? 1 : 0, num_sms, n_splits);
 }
 
 // ------------------------------------------------------------------------
@@ -453,6 +568,9 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   const long long units = (long long)B * H * p.n_qblocks;
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
+  p.n_splits = 1;  // no split-KV here: its partials would not fit a fixed array
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
   p.n_kv_tiles = n_kv_tiles;
   p.mode_stride = (n_kv_tiles + 7) / 8 * 8;
   p.v_mode = nullptr;

@@ -9,9 +9,15 @@
 //     LSE = -inf ("The safe softmax" section of the same profiling page).
 //
 // How (GB300 design, not the pages' Ampere blocking):
-//   * work unit = (batch*head, block of 2 x 128 query rows); CTAs are
-//     persistent and walk the units with a static stride, heaviest (latest,
-//     for causal) query blocks first;
+//   * work unit = (batch*head, block of 2 x 128 query rows, K/V split); CTAs
+//     are persistent and walk the units with a static stride, heaviest
+//     (latest, for causal) query blocks first.  With one split a unit covers
+//     all of its key tiles and writes O and LSE.  With several (split-KV, for
+//     grids with fewer units than SMs) the n key tiles a query block visits
+//     are cut into n_splits near-equal runs (split s: tiles
+//     [s*n/n_splits, (s+1)*n/n_splits)), and each writes its normalised
+//     partial output and log-sum-exp in fp32, which the combine kernel merges
+//     with the two-block rule of the same derivation;
 //   * warp 8 (one lane) is the TMA producer: Q tiles into two fixed buffers,
 //     K and V tiles into a STAGES-deep ring, all 128-byte swizzled panels of
 //     64 columns;
@@ -79,7 +85,10 @@ struct Params {
   float scale_log2;  // scale * log2(e)
   int causal;
   int n_qblocks;  // ceil(N / 256)
-  int n_units;    // B * H * n_qblocks
+  int n_units;    // B * H * n_qblocks * n_splits
+  int n_splits;    // K/V splits per query block (1: no split, O and LSE written directly)
+  float* o_part;   // n_splits > 1: [n_splits, B*H, N, D] fp32 O / l of each split
+  float* lse_part; // n_splits > 1: [n_splits, B*H, N] fp32 log-sum-exp of each split
   int n_kv_tiles; // ceil(N / 128)
   int mode_stride; // n_kv_tiles rounded up to 8: modes are read 8 at a time
   unsigned long long wait_limit_ns;
@@ -144,7 +153,8 @@ __host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool ab_bf16,
 // ------------------------------------------------------------------ work units
 struct Unit {
   int bh, b, r0;
-  int n0, n1;              // K/V tiles Q tile 0 / 1 visits (0: nothing to do)
+  int split, j0;           // K/V split and its first key tile
+  int n0, n1;              // K/V tiles Q tile 0 / 1 visits in this split (0: nothing to do)
   int min_lim0, min_lim1;  // smallest per-row key limit in each tile
   int kl;                  // effective key length of this batch entry
   int nkv;                 // max(n0, n1)
@@ -154,30 +164,53 @@ struct Unit {
   __device__ __forceinline__ bool valid(int t) const { return t ? valid1 : valid0; }
 };
 
+// Unit u = ((round * n_splits) + split) * B*H + bh: the query block of a round
+// is n_qblocks - 1 - round (latest, the heaviest under causal, first).
+
+// Key tiles that query tile `row0` visits over the whole key range, with
+// key length kl (clamped): every one of them holds a visible key for every
+// row of the tile.
+__device__ __forceinline__ int tile_kv_count(const Params& p, int row0, int kl) {
+  if (row0 >= p.N) return 0;
+  const int max_lim = p.causal ? min(kl, row0 + BM) : kl;
+  return max_lim > 0 ? (max_lim + BN - 1) / BN : 0;
+}
+
+
+template <bool SPLIT>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int kl_raw) {
   Unit w;
   const int BH = p.B * p.H;
-  const int round = u / BH;
+  const int ns = SPLIT ? p.n_splits : 1;
+  const int round = u / (BH * ns);
+  w.split = SPLIT ? (u / BH) % ns : 0;
   w.bh = u % BH;
   w.b = w.bh / p.H;
   const int qb = p.n_qblocks - 1 - round;  // latest (heaviest under causal) blocks first
   w.r0 = qb * (QT * BM);
   const int kl = kl_raw < 0 ? 0 : (kl_raw > p.N ? p.N : kl_raw);
   w.kl = kl;
-  int nn[QT], ml[QT];
+  int n_all[QT], ml[QT];
   bool vv[QT];
 #pragma unroll
   for (int t = 0; t < QT; ++t) {
     const int row0 = w.r0 + t * BM;
     vv[t] = row0 < p.N;
-    int max_lim = kl;
-    int min_lim = kl;
-    if (p.causal) {
-      max_lim = min(kl, row0 + BM);
-      min_lim = min(kl, row0 + 1);
-    }
-    nn[t] = (vv[t] && max_lim > 0) ? (max_lim + BN - 1) / BN : 0;
-    ml[t] = min_lim;
+    n_all[t] = tile_kv_count(p, row0, kl);  // tiles of the whole key range
+    ml[t] = p.causal ? min(kl, row0 + 1) : kl;
+  }
+  int nn[QT];
+  if constexpr (SPLIT) {
+    // this split's run of the block's key tiles: [j0, j1)
+    const int n_blk = max(n_all[0], n_all[1]);
+    w.j0 = w.split * n_blk / ns;
+    const int j1 = (w.split + 1) * n_blk / ns;
+#pragma unroll
+    for (int t = 0; t < QT; ++t) nn[t] = max(min(n_all[t], j1) - w.j0, 0);
+  } else {
+    w.j0 = 0;
+#pragma unroll
+    for (int t = 0; t < QT; ++t) nn[t] = n_all[t];
   }
   w.n0 = nn[0];
   w.n1 = nn[1];
@@ -215,7 +248,7 @@ struct UnitIter {
   __device__ __forceinline__ void load_next(const Params& p) {
     if (u_next < 0) return;
     kl_next = p.key_len ? __ldg(p.key_len + next_bh / p.H) : p.N;
-    mode_next = __ldg(p.v_mode + (size_t)next_bh * p.mode_stride);
+    mode_next = __ldg(p.v_mode + (size_t)next_bh * p.mode_stride);  // (split units read theirs at the unit start)
   }
   __device__ __forceinline__ void locate_next(const Params& p, int cta, int G) {
     r_next = r < 0 ? -1 : round_from(p, r + 1, cta, G);
@@ -308,7 +341,9 @@ __device__ __forceinline__ void static_for(F&& f) {
 
 
 // ------------------------------------------------------------------ the kernel
-template <int D>
+// SPLIT: the split-KV instantiation (p.n_splits > 1: partial outputs in fp32
+// for the combine kernel); without it the kernel writes O and LSE itself.
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const Params p) {
@@ -411,7 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       it.begin(p, cta, G);
       for (; ok && it.u >= 0; it.advance(p, cta, G)) {
         const int u = it.u;
-        const Unit w = decode_unit(p, u, it.kl_raw);
+        const Unit w = decode_unit<SPLIT>(p, u, it.kl_raw);
         it.at_tile(p, it.fetch_at);
         load_q(TileC<0>{}, w, u, q_use0);
         load_q(TileC<1>{}, w, u, q_use1);
@@ -427,11 +462,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t bit = 1u << (gk % 32u);
           two = ntiles == 2u ? (two | bit) : (two & ~bit);
           ++gk;
-          if (has_v) load_kv(&tmap_v, j, w.bh, full);
+          if (has_v) load_kv(&tmap_v, w.j0 + j, w.bh, full);
           if (has_k) {
             make_room(g, gk - 1u, u);
             if (!ok) break;
-            load_kv(&tmap_k, j + 1, w.bh, full);
+            load_kv(&tmap_k, w.j0 + j + 1, w.bh, full);
           }
         }
       }
@@ -502,7 +537,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       it.begin(p, cta, G);
       for (; ok && it.u >= 0; it.advance(p, cta, G)) {
         const int u = it.u;
-        const Unit w = decode_unit(p, u, it.kl_raw);
+        const Unit w = decode_unit<SPLIT>(p, u, it.kl_raw);
         if (w.nkv == 0) continue;  // (advance requests the next unit)
         auto kslot = [&](int j) { return (g + 2u * j) % C::STAGES; };
         auto vslot = [&](int j) { return (g + 2u * j + 1u) % C::STAGES; };
@@ -539,8 +574,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         kv_release();
 
-        const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride;
-        int vmode_next = it.mode0;
+        const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride + w.j0;
+        int vmode_next = SPLIT ? (int)__ldg(modes) : it.mode0;  // a split's first V tile is read here
         for (int j = 0; ok && j < w.nkv; ++j) {
           const uint32_t idesc_pv = vmode_next == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
           if (j + 1 < w.nkv) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
@@ -606,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     it.begin(p, cta, G);
     for (; ok && it.u >= 0; it.advance(p, cta, G)) {
       const int u = it.u;
-      const Unit w = decode_unit(p, u, it.kl_raw);
+      const Unit w = decode_unit<SPLIT>(p, u, it.kl_raw);
       if (!w.valid(t)) continue;
       const int n_t = w.n(t);
       const int min_lim = w.min_lim(t);
@@ -614,6 +649,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = row < p.N;
       const size_t row_flat = (size_t)w.bh * (size_t)p.N + (size_t)row;
       if (n_t == 0) {
+        // split-KV: this split holds none of the tile's keys (the combine
+        // kernel reads only the splits that do)
+        if constexpr (SPLIT) continue;
         // no visible key at all: O = 0, LSE = -inf
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
@@ -623,15 +661,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      const int lim = p.causal ? min(w.kl, row + 1) : w.kl;  // keys [0, lim) are visible
+      // keys [0, lim) are visible; both limits are taken relative to the
+      // split's first key, so the tile loop below counts from 0
+      const int lim = (p.causal ? min(w.kl, row + 1) : w.kl) - w.j0 * BN;
+      const int min_lim_s = min_lim - w.j0 * BN;
       float m_ref = -INFINITY;
       float l = 0.0f;
-      const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride;
+      const uint8_t* modes = p.v_mode + (size_t)w.bh * p.mode_stride + w.j0;
       int vmode_next = it.mode0;
 
       for (int j = 0; j < n_t; ++j) {
-        const int vmode = vmode_next;
-        if (j + 1 < n_t) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+        int vmode;
+        if constexpr (SPLIT) {
+          // storage type of V_j, needed only once P is formed (the load's
+          // latency hides behind the S wait and the exponentials)
+          vmode = __ldg(modes + j);
+        } else {
+          vmode = vmode_next;
+          if (j + 1 < n_t) vmode_next = __ldg(modes + j + 1);  // fetched a tile ahead
+        }
         it.at_tile(p, j);
         ok = wait_bar(waiter, bar_s_full, s_cnt & 1u, C::B_S_FULL + t, u);
         ok = __all_sync(0xffffffffu, ok);
@@ -639,7 +687,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++s_cnt;
         tc_fence_after();
 
-        const bool masked_tile = (j + 1) * BN > min_lim;
+        const bool masked_tile = (j + 1) * BN > min_lim_s;
         const int vis_n = lim - j * BN;  // columns [0, vis_n) visible
         // row max: from the TMEM load's max reduction on tiles without a mask;
         // with a mask, in registers over the visible columns only
@@ -772,30 +820,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++o_cnt;
       tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-      // read O 64 columns at a time, pack to bf16 and store each half; O is
-      // handed back to the MMA issuer once both halves are in registers
-      uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
+      if constexpr (SPLIT) {
+        // this split's O / l and log-sum-exp in fp32, for the combine kernel;
+        // O is handed back to the MMA issuer once both halves are in registers
+        const size_t orow = (size_t)w.split * (size_t)(p.B * p.H) * (size_t)p.N + row_flat;
 #pragma unroll
-      for (int hcol = 0; hcol < D / 64; ++hcol) {
-        uint32_t ov[64];
-        tmem_ld64(o_addr + 64u * hcol, ov);
-        tmem_ld_wait(ov);
-        uint32_t ob[32];
+        for (int hcol = 0; hcol < D / 64; ++hcol) {
+          uint32_t ov[64];
+          tmem_ld64(o_addr + 64u * hcol, ov);
+          tmem_ld_wait(ov);
+          if (hcol == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar_o_empty);
+          }
+          if (row_ok) {
+            float4* dstf = reinterpret_cast<float4*>(p.o_part + orow * D) + 16 * hcol;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          ob[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
-        if (hcol == D / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive(bar_o_empty);
+            for (int i = 0; i < 16; ++i)
+              dstf[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l, __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                    __uint_as_float(ov[4 * i + 2]) * inv_l, __uint_as_float(ov[4 * i + 3]) * inv_l);
+          }
+        }
+        if (row_ok) p.lse_part[orow] = (m_ref * c + __log2f(l)) * 0.69314718055994531f;  // l > 0 here
+      } else {
+        // read O 64 columns at a time, pack to bf16 and store each half; O is
+        // handed back to the MMA issuer once both halves are in registers
+        uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
+#pragma unroll
+        for (int hcol = 0; hcol < D / 64; ++hcol) {
+          uint32_t ov[64];
+          tmem_ld64(o_addr + 64u * hcol, ov);
+          tmem_ld_wait(ov);
+          uint32_t ob[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ob[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l, __uint_as_float(ov[2 * i + 1]) * inv_l);
+          if (hcol == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar_o_empty);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+          }
         }
         if (row_ok) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+          const float lse = (l > 0.0f) ? (m_ref * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          p.lse[row_flat] = lse;
         }
-      }
-      if (row_ok) {
-        const float lse = (l > 0.0f) ? (m_ref * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        p.lse[row_flat] = lse;
       }
     }
   }

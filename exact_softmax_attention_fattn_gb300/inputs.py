@@ -142,7 +142,9 @@ def make_inputs(w: Workload) -> Inputs:
     return Inputs(w, q, k, v, key_len)
 
 
-# The five workloads the attention forward is measured and checked on.
+# The five workloads the attention forward is measured and checked on, and a
+# long causal sequence with few heads: fewer blocks of 256 query rows (128)
+# than a GB300 has SMs (152), the shape split-KV is for.
 WORKLOADS: dict[str, Workload] = {
     "b1h1n128d64": Workload("b1h1n128d64", 1, 1, 128, 64, False, 0),
     "b1h1n128d64_causal": Workload("b1h1n128d64_causal", 1, 1, 128, 64, True, 0),
@@ -153,6 +155,7 @@ WORKLOADS: dict[str, Workload] = {
         "b8h16n2048d128_keylen", 8, 16, 2048, 128, False, 4,
         qk_sigma=2.0, key_len_range=(1024, 2048),
     ),
+    "b1h2n16384d128_causal": Workload("b1h2n16384d128_causal", 1, 2, 16384, 128, True, 5),
 }
 
 HEADLINE = "b2h16n4096d128_causal"

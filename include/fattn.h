@@ -74,10 +74,19 @@ typedef enum {
  * the operand type of the P V product (fp16 per 128-row tile where V's
  * range allows, else bf16), so the probabilities P are rounded to fp16.
  *
+ * Split-KV: when the problem has fewer blocks of 256 query rows than the GPU
+ * has SMs, the call may split each block's key range (the split count that
+ * fattn_splitkv_plan(B, H, N, causal, SMs, 0) returns) and merge the
+ * splits' partial results with the two-block rule ("understand-
+ * flashattention", two-block online-softmax derivation); the scratch then
+ * grows by n_splits*B*H*N*(d+1)*4 bytes (fp32 partial O and LSE).  The
+ * result is the same function, rounded once to bf16 at the end.
+ *
  * Asynchrony: the call validates its arguments synchronously, then enqueues
- * two kernels on `stream` (the V pre-pass and the attention kernel) and
- * returns without synchronising.  Time-outs of the kernel's bounded waits
- * are reported later by fattn_last_error().
+ * two kernels on `stream` (the V pre-pass and the attention kernel; a third,
+ * the split-KV combine, when it splits) and returns without synchronising.
+ * Time-outs of the kernel's bounded waits are reported later by
+ * fattn_last_error().
  *
  * Returns FATTN_OK, FATTN_ERR_INVALID_ARG (null pointer with B*H*N > 0,
  * negative size, misaligned pointer, host pointer, non-finite or negative
@@ -122,6 +131,40 @@ FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void*
                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                         int causal, const int32_t* key_len, void* stream);
 
+/*
+ * fattn_fwd_splitkv: fattn_fwd with the split-KV choice made by the caller.
+ *
+ *   n_splits  0: the library's choice (exactly fattn_fwd); 1: no split (the
+ *             attention kernel writes O and LSE itself); k > 1: min(k,
+ *             ceil(N/128)) splits.  The n key tiles of 128 that a block of
+ *             256 query rows visits (after the causal and key_len masks) are
+ *             cut into near-equal runs, split s taking tiles
+ *             [s*n/k, (s+1)*n/k); each split's normalised output and
+ *             log-sum-exp over its keys are kept in fp32 and merged by a
+ *             combine kernel:
+ *                 LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+ *             over the splits that hold keys of the row.
+ *             Negative: FATTN_ERR_INVALID_ARG.
+ *
+ * Every other argument, the layouts, ownership and errors are those of
+ * fattn_fwd; the scratch is as described there for the split count used.
+ */
+FATTN_API int fattn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                int N, int d, float scale, int causal, const int32_t* key_len, int n_splits,
+                                void* stream);
+
+/*
+ * fattn_splitkv_plan: the split count the forward uses, computed on the host
+ * alone (no GPU, no CUDA call).  n_splits as for fattn_fwd_splitkv: k > 0
+ * returns min(k, ceil(N/128)); 0 returns the library's choice: 1 whenever
+ * B*H*ceil(N/256) >= num_sms, else the count up to 16 with the least
+ * estimated time of the kernel's static schedule over num_sms SMs (each work
+ * unit's key tiles plus a fixed per-unit cost, plus the combine pass when
+ * split; all N keys assumed visible apart from the causal mask).  Returns 0
+ * for B, H, N or num_sms <= 0 or n_splits < 0.
+ */
+FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits);
+
 /* A static, human-readable name for a status code. */
 FATTN_API const char* fattn_status_string(int status);
 
@@ -150,7 +193,8 @@ FATTN_API int fattn_last_error(void* stream, int* detail);
  * driver's allocation locks.  The paper has no counterpart; this is a
  * property of the library, not of the method.
  *
- * Arguments, layouts, semantics and results are exactly those of fattn_fwd.
+ * Arguments, layouts, semantics and results are exactly those of fattn_fwd,
+ * except that it never splits the key range (split-KV; see fattn_fwd).
  * Instead of per-call scratch from a pool, the call uses one static device
  * array of FATTN_NOALLOC_SCRATCH_BYTES (+256) bytes compiled into the
  * library, and calls no cudaMalloc, cudaFree or allocating routine.

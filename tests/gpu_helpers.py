@@ -53,7 +53,7 @@ def guards_intact(o_buf, l_buf) -> bool:
     return ok_o and ok_l
 
 
-def run_gpu(x, dev, causal=None, scale=None, key_len="default", check_guards=True):
+def run_gpu(x, dev, causal=None, scale=None, key_len="default", check_guards=True, n_splits=None):
     """Run the kernel on Inputs x; returns (o float64 numpy, lse float64 numpy)."""
     import torch
 
@@ -67,7 +67,7 @@ def run_gpu(x, dev, causal=None, scale=None, key_len="default", check_guards=Tru
     B, H, N, d = x.q.shape
     o_buf, l_buf, o, lse = guarded_outputs(B, H, N, d, dev)
     kl_t = None if kl is None else torch.from_numpy(np.asarray(kl, dtype=np.int32)).to(dev)
-    binding.forward_into(q, k, v, o, lse, causal=causal, scale=scale, key_len=kl_t)
+    binding.forward_into(q, k, v, o, lse, causal=causal, scale=scale, key_len=kl_t, n_splits=n_splits)
     st, detail = binding.last_error()
     assert st == binding.FATTN_OK, f"kernel reported {binding.status_string(st)} {detail}"
     torch.cuda.synchronize()

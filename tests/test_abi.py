@@ -159,3 +159,18 @@ def test_forward_without_gpu_raises():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(binding.FattnError):
         binding.forward(q, q, q)
+
+
+def test_splitkv_argument_checks(lib):
+    """fattn_fwd_splitkv validates like fattn_fwd, plus a negative split count."""
+    def callk(n_splits, **kw):
+        a = dict(B=1, H=1, N=128, d=64, scale=0.125, causal=0)
+        a.update(kw)
+        return binding.fwd_raw(FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"], a["scale"],
+                               a["causal"], None, None, n_splits)
+
+    assert callk(-1) == binding.FATTN_ERR_INVALID_ARG
+    assert callk(2, B=0) == binding.FATTN_OK
+    assert callk(2, d=96) == binding.FATTN_ERR_UNSUPPORTED
+    assert callk(2, scale=float("nan")) == binding.FATTN_ERR_INVALID_ARG
+    assert callk(0, N=-1) == binding.FATTN_ERR_INVALID_ARG

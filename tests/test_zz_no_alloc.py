@@ -31,7 +31,9 @@ def _noalloc():
 
 
 def _check_against_fattn_fwd(w, dev, key_len=None):
-    """Two no-alloc calls in a row, each compared with fattn_fwd's result."""
+    """Two no-alloc calls in a row, each bit-identical to the forward without
+    split-KV (fattn_fwd_splitkv with one split: the same kernel and scratch
+    layout; the no-alloc entry point never splits)."""
     import torch
 
     x = make_inputs(w)
@@ -40,7 +42,7 @@ def _check_against_fattn_fwd(w, dev, key_len=None):
     B, H, N, d = x.q.shape
     o_ref = torch.empty_like(q)
     lse_ref = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    binding.forward_into(q, k, v, o_ref, lse_ref, causal=w.causal, scale=w.softmax_scale, key_len=kl)
+    binding.forward_into(q, k, v, o_ref, lse_ref, causal=w.causal, scale=w.softmax_scale, key_len=kl, n_splits=1)
     fn = _noalloc()
     stream = torch.cuda.current_stream(dev).cuda_stream
     outs = []
@@ -54,6 +56,8 @@ def _check_against_fattn_fwd(w, dev, key_len=None):
     torch.cuda.synchronize(dev)
     ref = (o_ref.float().cpu().numpy().astype(np.float64), lse_ref.cpu().numpy().astype(np.float64))
     for o, lse in outs:
+        np.testing.assert_array_equal(o.view(torch.int16).cpu().numpy(), o_ref.view(torch.int16).cpu().numpy())
+        np.testing.assert_array_equal(lse.cpu().numpy(), lse_ref.cpu().numpy())
         compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), *ref,
                 what=f"no-alloc {w.name}")
 
