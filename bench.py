@@ -8,6 +8,10 @@ scores, masks, online softmax, correction, PV, epilogue) over the workload's
 synthetic inputs, already resident in HBM.  Between timed steps the L2 cache
 is flushed by writing a 256 MiB buffer; each step's kernel is timed with CUDA
 events on the stream it is launched on, and the steps' times are summed.
+nvidia-smi samples the clocks from the start of the warm-up, which runs the
+same (untimed) step until the GPU has been under this load for 0.5 s
+("untimed_steps"), through the timed steps: the timed region alone is a few
+milliseconds, far shorter than the sampling interval.
 
 Default workload: B=2, H=16, N=4096, d=128, causal, bf16, seed 2.  Metric:
 attention forward TFLOP/s with causal FLOPs counted at half (4*B*H*N^2*d/2).
@@ -24,6 +28,11 @@ workload, in the same metric.
 --pass bwd times the backward instead (fattn_bwd: dQ, dK, dV from dO and the
 forward's O and LSE, which are computed once before the timed region), with
 FLOPs counted as 2.5x the forward's (five GEMMs of the forward's size).
+
+The forward splits each query block's key range (split-KV, with a combine
+kernel) when the library's plan says so -- on shapes with fewer blocks of 256
+query rows than SMs; --splits K forces K splits (1: none), and the split count
+used is reported in config.kv_splits.
 """
 from __future__ import annotations
 
@@ -151,6 +160,28 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": float(max(power)) if power else None}
 
 
+def warm_up(step, flush, warmup: int, sampler, dev, load_seconds: float = 0.5) -> int:
+    """The untimed warm-up: `warmup` steps (each after an L2 flush), extended
+    with more untimed steps of the same work until the clock sampler (started
+    before it) has watched the GPU under this load for `load_seconds`, so the
+    clock samples describe the clocks the timed steps run at.  Returns the
+    number of untimed steps run."""
+    import torch
+
+    if sampler:
+        sampler.start()
+    t_end = time.perf_counter() + (load_seconds if sampler else 0.0)
+    n = 0
+    while n < warmup or time.perf_counter() < t_end:
+        flush.fill_(1)
+        step()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize(dev)  # keep the queue short so the load tracks the wall clock
+    torch.cuda.synchronize(dev)
+    return n
+
+
 # ---------------------------------------------------------------- oracle leg
 def oracle_sample(workload: str, seconds: float, x=None):
     """Time the fp64 oracle on a bounded sample of query rows; returns
@@ -258,24 +289,22 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     flops = causal_flops(w, x.key_len)
 
     def step():
-        binding.forward_into(q, k, v, o, lse, causal=w.causal, scale=w.softmax_scale, key_len=kl)
+        binding.forward_into(q, k, v, o, lse, causal=w.causal, scale=w.softmax_scale, key_len=kl, n_splits=args.splits)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_splits = binding.splitkv_plan(w.B, w.H, w.N, w.causal, sms, args.splits or 0)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    untimed = warm_up(step, flush, args.warmup, sampler, dev)
     st, detail = binding.last_error(stream)
     if st != binding.FATTN_OK:
         raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
 
-    sampler = ClockSampler(local_rank) if rank == 0 else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
@@ -299,12 +328,13 @@ def our_arm(args, rank: int, world: int, local_rank: int):
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         klh = None if x.key_len is None else torch.from_numpy(x.key_len)
         for _ in range(2):
-            binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh)
+            binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh, n_splits=args.splits)
         n_e2e = max(3, min(args.steps, 10))
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(n_e2e):
-            oh, lh = binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh)
+            oh, lh = binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh,
+                                     n_splits=args.splits)
         torch.cuda.synchronize(dev)
         e2e_s = (time.perf_counter() - t0) / n_e2e
         h2d = 3 * q.numel() * 2 + (0 if klh is None else klh.numel() * 4)
@@ -324,20 +354,23 @@ def our_arm(args, rank: int, world: int, local_rank: int):
                "seconds": round(dt, 2)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "untimed_steps": untimed, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64/Box-Muller, bf16-rounded)",
         "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "key_padding": x.key_len is not None, "flops_per_step": flops,
+                   "kv_splits": n_splits, "kv_split_choice": "library" if args.splits is None else "forced",
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "traffic": traffic},
+                     "traffic": traffic if n_splits == 1 else None},
         "pct_of_bf16_peak": 100.0 * achieved / peak,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,  # V pre-pass + attention kernel per step
-        "kernel": KERNEL_NAME,
+        # V pre-pass + attention kernel per step, + the split-KV combine when split
+        "gpu_launches": (2 + (n_splits > 1)) * args.steps,
+        "kernel": KERNEL_NAME + (" + fattn_splitkv_combine_kernel" if n_splits > 1 else ""),
         "kernel_ms": {"min": min(kernel_ms), "median": float(np.median(kernel_ms)), "max": max(kernel_ms)},
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
@@ -375,19 +408,14 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
     def step():
         binding.backward_into(q, k, v, o, lse, go, dq, dk, dv, causal=w.causal, scale=w.softmax_scale, key_len=kl)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    untimed = warm_up(step, flush, args.warmup, sampler, dev)
     st, detail = binding.last_error(stream)
     if st != binding.FATTN_OK:
         raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
-    sampler = ClockSampler(local_rank) if rank == 0 else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
@@ -441,6 +469,7 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
     line = {
         "metric": "attention bwd TFLOP/s (causal-adjusted, 2.5x forward FLOPs) and % of GB300 bf16 dense peak",
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "untimed_steps": untimed,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded SplitMix64/Box-Muller, bf16-rounded)",
         "config": {"workload": args.workload, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
@@ -472,6 +501,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="forward: force this many key splits per query block (split-KV; 1 = none); "
+                         "default: the library's choice")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

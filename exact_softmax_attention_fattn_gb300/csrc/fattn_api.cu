@@ -199,6 +199,16 @@ double split_cost(int B, int H, int N, int causal, int num_sms, int splits) {
   return *std::max_element(load.begin(), load.end()) + (splits > 1 ? kCombineSteps : 0.0);
 }
 
+// The searched plans of recent shapes: the search simulates the schedule for
+// every candidate, too slow to repeat on each call of a hot loop.
+struct PlanEntry {
+  int B, H, N, causal, num_sms, splits;
+};
+constexpr int kPlanCache = 64;
+std::mutex g_plan_mu;
+PlanEntry g_plans[kPlanCache];
+int g_plans_used = 0, g_plans_next = 0;
+
 // K/V splits per query block.  requested > 0: that many, at most one per key
 // tile; 0: the cheapest by split_cost, searched only when the query blocks
 // alone leave SMs idle.
@@ -206,8 +216,16 @@ int plan_splits(int B, int H, int N, int causal, int num_sms, int requested) {
   const int n_kv = (N + fattn::BN - 1) / fattn::BN;
   const long long units = (long long)B * H * ((N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM));
   if (requested > 0) return std::min(requested, n_kv);
+  if (units >= num_sms || n_kv < 2) return 1;
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    for (int i = 0; i < g_plans_used; ++i) {
+      const PlanEntry& e = g_plans[i];
+      if (e.B == B && e.H == H && e.N == N && e.causal == causal && e.num_sms == num_sms) return e.splits;
+    }
+  }
   int best = 1;
-  if (units < num_sms && n_kv >= 2) {
+  {
     double best_cost = split_cost(B, H, N, causal, num_sms, 1);
     for (int sp = 2; sp <= std::min(n_kv, kMaxSplits); ++sp) {
       const double cst = split_cost(B, H, N, causal, num_sms, sp);
@@ -217,6 +235,10 @@ int plan_splits(int B, int H, int N, int causal, int num_sms, int requested) {
       }
     }
   }
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plans[g_plans_next] = PlanEntry{B, H, N, causal, num_sms, best};
+  g_plans_next = (g_plans_next + 1) % kPlanCache;
+  if (g_plans_used < kPlanCache) ++g_plans_used;
   return best;
 }
 
@@ -249,11 +271,10 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
     fattn::fattn_fwd_kernel<D, false><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   if (p.n_splits > 1) {
-    constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 4);
-    const long long n_rows = (long long)BH * p.N;
-    fattn::fattn_splitkv_combine_kernel<D>
-        <<<(unsigned)((n_rows + rows_per_block - 1) / rows_per_block), fattn::COMBINE_THREADS, 0, stream>>>(
-            p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.causal, p.n_splits);
+    constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 16);
+    const dim3 cgrid((unsigned)((p.N + rows_per_block - 1) / rows_per_block), (unsigned)(BH < 65535 ? BH : 65535));
+    fattn::fattn_splitkv_combine_kernel<D><<<cgrid, fattn::COMBINE_THREADS, 0, stream>>>(
+        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.causal, p.n_splits);
     if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   }
   return FATTN_OK;

@@ -17,9 +17,10 @@
 // LSE = -inf.
 //
 // HBM-bound: per row, (splits with a partial) * (D * 4 + 4) bytes read,
-// D * 2 + 4 written.
-// One thread per 4 columns of a row, so a warp reads whole 512-byte rows
-// (D = 128) or two 256-byte rows (D = 64).
+// D * 2 + 4 written.  Grid (row blocks, heads); D / 16 threads per row, each
+// holding 16 columns as 4 float4 loads interleaved with its neighbours' (the
+// i-th load of the row's threads covers 128 contiguous bytes), so the
+// per-row scalar work (limits, split runs, weights) is shared by few threads.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,46 +43,71 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
                                  __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                  const int32_t* __restrict__ key_len, int B, int H, int N, int causal,
                                  int n_splits) {
-  constexpr int TPR = D / 4;  // threads per row
+  constexpr int VPT = 4;            // float4 per thread and split
+  constexpr int TPR = D / (4 * VPT);  // threads per row
   constexpr int ROWS = COMBINE_THREADS / TPR;
-  const long long n_rows = (long long)B * H * N;
-  const long long rg = (long long)blockIdx.x * ROWS + threadIdx.x / TPR;  // row over all heads
-  const int c4 = threadIdx.x % TPR;                                       // column group
-  if (rg >= n_rows) return;
-  const int bh = (int)(rg / N);
-  const int row = (int)(rg % N);
-  int kl = key_len ? key_len[bh / H] : N;
-  kl = kl < 0 ? 0 : (kl > N ? N : kl);
-  const int blk0 = row / 256 * 256;
-  const int n_blk = max(combine_tiles_of(blk0, N, kl, causal), combine_tiles_of(blk0 + 128, N, kl, causal));
-  const int n_t = combine_tiles_of(row / 128 * 128, N, kl, causal);
-  uint2* dst = reinterpret_cast<uint2*>(o + rg * D) + c4;
-  if (n_t == 0) {
-    *dst = make_uint2(0u, 0u);
-    if (c4 == 0) lse[rg] = -INFINITY;
-    return;
+  const int row = blockIdx.x * ROWS + threadIdx.x / TPR;  // grid: (row blocks, heads)
+  const int c4 = threadIdx.x % TPR;                       // float4 columns c4 + TPR * i, i < VPT
+  if (row >= N) return;
+  const int BH = B * H;
+  const size_t stride = (size_t)BH * N;  // rows between two splits' partials
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    int kl = key_len ? __ldg(key_len + bh / H) : N;
+    kl = kl < 0 ? 0 : (kl > N ? N : kl);
+    const int blk0 = row / 256 * 256;
+    const int n_blk = max(combine_tiles_of(blk0, N, kl, causal), combine_tiles_of(blk0 + 128, N, kl, causal));
+    const int n_t = combine_tiles_of(row / 128 * 128, N, kl, causal);
+    const size_t rg = (size_t)bh * N + row;
+    uint2* dst = reinterpret_cast<uint2*>(o + rg * D) + c4;
+    if (n_t == 0) {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) dst[TPR * i] = make_uint2(0u, 0u);
+      if (c4 == 0) lse[rg] = -INFINITY;
+      continue;
+    }
+    // one pass over the splits holding keys of this row: split s covers key
+    // tiles [j0, j1) = [s*n_blk/n_splits, (s+1)*n_blk/n_splits) and holds
+    // keys of the row iff j0 < j1 and j0 < n_t.  The running merge is the
+    // two-block rule applied split after split (max m, sum of e^(L_s - m),
+    // output weighted alike), rescaled when m grows.
+    float m = -INFINITY, sum = 0.0f;
+    float4 acc[VPT];
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int j0 = 0;
+#pragma unroll 2
+    for (int s = 0; s < n_splits && j0 < n_t; ++s) {
+      const int j1 = (s + 1) * n_blk / n_splits;
+      if (j1 > j0) {
+        const float ls = lse_part[s * stride + rg];
+        const float4* src = reinterpret_cast<const float4*>(o_part + (s * stride + rg) * D) + c4;
+        float4 v[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) v[i] = src[TPR * i];
+        const float mn = fmaxf(m, ls);
+        const float r = expf(m - mn);  // 0 for the first split (m = -inf)
+        const float w = expf(ls - mn);
+        sum = fmaf(sum, r, w);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          acc[i].x = fmaf(acc[i].x, r, w * v[i].x);
+          acc[i].y = fmaf(acc[i].y, r, w * v[i].y);
+          acc[i].z = fmaf(acc[i].z, r, w * v[i].z);
+          acc[i].w = fmaf(acc[i].w, r, w * v[i].w);
+        }
+        m = mn;
+      }
+      j0 = j1;
+    }
+    const float inv = 1.0f / sum;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
+      dst[TPR * i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+    if (c4 == 0) lse[rg] = m + logf(sum);
   }
-  const long long stride = n_rows;  // between splits, in rows
-  float m = -INFINITY;
-  // split s holds keys of this row iff its run [s*n_blk/n_splits, ...) starts below n_t
-  for (int s = 0; s < n_splits && s * n_blk / n_splits < n_t; ++s)
-    if ((s + 1) * n_blk / n_splits > s * n_blk / n_splits) m = fmaxf(m, lse_part[s * stride + rg]);
-  float sum = 0.0f, a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-  for (int s = 0; s < n_splits && s * n_blk / n_splits < n_t; ++s) {
-    if ((s + 1) * n_blk / n_splits == s * n_blk / n_splits) continue;  // an empty run
-    const float w = expf(lse_part[s * stride + rg] - m);
-    const float4 v = reinterpret_cast<const float4*>(o_part + (s * stride + rg) * D)[c4];
-    sum += w;
-    a0 = fmaf(w, v.x, a0);
-    a1 = fmaf(w, v.y, a1);
-    a2 = fmaf(w, v.z, a2);
-    a3 = fmaf(w, v.w, a3);
-  }
-  const float inv = 1.0f / sum;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 * inv, a1 * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(a2 * inv, a3 * inv);
-  *dst = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-  if (c4 == 0) lse[rg] = m + logf(sum);
 }
 
 }  // namespace fattn
