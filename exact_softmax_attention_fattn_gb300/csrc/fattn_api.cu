@@ -58,21 +58,23 @@ unsigned long long wait_limit_ns() {
 // Sets the kernel's shared-memory limit and checks that it was compiled with
 // the register count its setmaxnreg split assumes (a split larger than the
 // launch allocation would never be granted).
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool FULL>
 int configure_fwd_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(fattn::fattn_fwd_kernel<D, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)fattn::Cfg<D>::SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(fattn::fattn_fwd_kernel<D, SPLIT, FULL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fattn::Cfg<D>::SMEM_BYTES);
   if (e != cudaSuccess) return FATTN_ERR_CUDA;
   cudaFuncAttributes a;
-  if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D, SPLIT>) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D, SPLIT, FULL>) != cudaSuccess) return FATTN_ERR_CUDA;
   if (a.numRegs != fattn::LAUNCH_REGS) return FATTN_ERR_UNSUPPORTED;
   return FATTN_OK;
 }
 
 template <int D>
 int configure_kernel() {
-  int rc = configure_fwd_kernel<D, false>();
-  if (rc == FATTN_OK) rc = configure_fwd_kernel<D, true>();
+  int rc = configure_fwd_kernel<D, false, true>();
+  if (rc == FATTN_OK) rc = configure_fwd_kernel<D, true, true>();
+  if (rc == FATTN_OK) rc = configure_fwd_kernel<D, false, false>();
+  if (rc == FATTN_OK) rc = configure_fwd_kernel<D, true, false>();
   if (rc != FATTN_OK) return rc;
   if (cudaFuncSetAttribute(fattn::fattn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)fattn::BwdCfg<D>::SMEM_BYTES) != cudaSuccess ||
@@ -137,7 +139,8 @@ bool is_device_pointer(const void* ptr) {
 
 // [B*H, N, d] 16-bit elements viewed as a 3-D tensor: x = head dim (innermost),
 // y = row, z = batch*head.  Boxes of 64 x 128 x 1 with 128-byte swizzle; rows
-// past N read as zero.
+// past N and columns past d (head dims below the kernel's 64 or 128) read as
+// zero.
 int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType type) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2ull, (cuuint64_t)N * (cuuint64_t)d * 2ull};
@@ -150,6 +153,11 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Head dims the kernels run: multiples of 8 (rows of 16-byte vectors, TMA
+// strides in 16-byte units) up to 128, computed in the 64- or 128-column
+// instantiation with the columns past d read as zeros by the tensor maps.
+bool head_dim_supported(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
 
 // Scratch of one call: V in its per-tile storage type, then one mode byte per
 // tile, each head's row of modes padded to a multiple of 8 bytes; with
@@ -249,32 +257,46 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
             cudaStream_t stream) {
   const int BH = p.B * p.H;
   uint8_t* v16 = reinterpret_cast<uint8_t*>(scratch);
-  uint8_t* modes = v16 + round_up((size_t)BH * (size_t)p.N * D * 2u, 256);
+  uint8_t* modes = v16 + round_up((size_t)BH * (size_t)p.N * (size_t)p.hd * 2u, 256);
   p.v_mode = modes;
   if (p.n_splits > 1) {
     uint8_t* part = modes + round_up((size_t)BH * round_up((size_t)p.n_kv_tiles, 8), 256);
     p.o_part = reinterpret_cast<float*>(part);
-    p.lse_part = reinterpret_cast<float*>(part + round_up((size_t)p.n_splits * BH * (size_t)p.N * D * 4u, 256));
+    p.lse_part =
+        reinterpret_cast<float*>(part + round_up((size_t)p.n_splits * BH * (size_t)p.N * (size_t)p.hd * 4u, 256));
   }
   CUtensorMap mq, mk, mv;
-  if (encode_map(&mq, q, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
-      encode_map(&mk, k, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
-      encode_map(&mv, v16, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) != FATTN_OK)
+  if (encode_map(&mq, q, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mv, v16, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) != FATTN_OK)
     return FATTN_ERR_CUDA;
   const long long prepass_blocks = (long long)BH * p.n_kv_tiles;
-  fattn::fattn_v_prepass_kernel<D><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
-      reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.n_kv_tiles, p.mode_stride);
-  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  if (p.n_splits > 1)
-    fattn::fattn_fwd_kernel<D, true><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  if (p.hd == D)
+    fattn::fattn_v_prepass_kernel<D, true><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
+        p.mode_stride);
   else
-    fattn::fattn_fwd_kernel<D, false><<<grid, fattn::NUM_THREADS, fattn::Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+    fattn::fattn_v_prepass_kernel<D, false><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
+        p.mode_stride);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  constexpr uint32_t smem = fattn::Cfg<D>::SMEM_BYTES;
+  constexpr int nt = fattn::NUM_THREADS;
+  const bool full = p.hd == D;
+  if (p.n_splits > 1 && full)
+    fattn::fattn_fwd_kernel<D, true, true><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
+  else if (p.n_splits > 1)
+    fattn::fattn_fwd_kernel<D, true, false><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
+  else if (full)
+    fattn::fattn_fwd_kernel<D, false, true><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
+  else
+    fattn::fattn_fwd_kernel<D, false, false><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   if (p.n_splits > 1) {
     constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 16);
     const dim3 cgrid((unsigned)((p.N + rows_per_block - 1) / rows_per_block), (unsigned)(BH < 65535 ? BH : 65535));
     fattn::fattn_splitkv_combine_kernel<D><<<cgrid, fattn::COMBINE_THREADS, 0, stream>>>(
-        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.causal, p.n_splits);
+        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.hd, p.causal, p.n_splits);
     if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   }
   return FATTN_OK;
@@ -306,7 +328,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       (key_len && !aligned(key_len, 4)))
@@ -329,6 +351,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.B = B;
   p.H = H;
   p.N = N;
+  p.hd = d;
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.causal = causal ? 1 : 0;
@@ -353,7 +376,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     cudaGetLastError();
     return FATTN_ERR_CUDA;
   }
-  rc = d == 64 ? enqueue<64>(q, k, v, p, scratch, grid, s) : enqueue<128>(q, k, v, p, scratch, grid, s);
+  rc = d <= 64 ? enqueue<64>(q, k, v, p, scratch, grid, s) : enqueue<128>(q, k, v, p, scratch, grid, s);
   if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }
@@ -390,16 +413,21 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
   p.lse2 = lse2;
   p.delta = delta;
   const long long prep_threads = n_rows * (D / 8);
-  fattn::fattn_bwd_prep_kernel<D>
-      <<<(unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS), fattn::PREP_THREADS, 0, stream>>>(
-          reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad,
-          n_rows);
+  const unsigned prep_blocks = (unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS);
+  if (p.hd == D)
+    fattn::fattn_bwd_prep_kernel<D, true><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        n_rows);
+  else
+    fattn::fattn_bwd_prep_kernel<D, false><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        n_rows);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo;
-  if (encode_map(&mq, q, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
-      encode_map(&mk, k, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
-      encode_map(&mv, v, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
-      encode_map(&mdo, dout, BH, p.N, D, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
+  if (encode_map(&mq, q, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mv, v, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mdo, dout, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
     return FATTN_ERR_CUDA;
   const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
   fattn::fattn_bwd_dkdv_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo,
@@ -420,7 +448,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   const void* ptrs16[8] = {q, k, v, o, dout, dq, dk, dv};
   for (const void* ptr : ptrs16)
@@ -445,6 +473,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   p.N = N;
   p.n_tiles = (N + 127) / 128;
   p.N_pad = p.n_tiles * 128;
+  p.hd = d;
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.causal = causal ? 1 : 0;
@@ -460,7 +489,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
     return FATTN_ERR_CUDA;
   }
   float* rf = reinterpret_cast<float*>(rows);
-  rc = d == 64 ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s) : enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s);
+  rc = d <= 64 ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s) : enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s);
   if (cudaFreeAsync(rows, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }
@@ -555,7 +584,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   const int n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
   if ((long long)B * H * ((n_kv_tiles + 7) / 8 * 8) > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
@@ -582,6 +611,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   p.B = B;
   p.H = H;
   p.N = N;
+  p.hd = d;
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.causal = causal ? 1 : 0;
@@ -600,5 +630,5 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the error word must start at zero for this call; the V copy and modes are fully rewritten
   if (cudaMemsetAsync(p.err, 0, 4 * sizeof(int), s) != cudaSuccess) return FATTN_ERR_CUDA;
-  return d == 64 ? enqueue<64>(q, k, v, p, ns->scratch, grid, s) : enqueue<128>(q, k, v, p, ns->scratch, grid, s);
+  return d <= 64 ? enqueue<64>(q, k, v, p, ns->scratch, grid, s) : enqueue<128>(q, k, v, p, ns->scratch, grid, s);
 }

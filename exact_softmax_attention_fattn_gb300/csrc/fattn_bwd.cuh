@@ -50,6 +50,7 @@ struct BwdParams {
   const int32_t* key_len;  // [B] or nullptr
   int* err;                // int[4]
   int B, H, N, N_pad;
+  int hd;            // head dim of the tensors (a multiple of 8, <= D); columns past it are read as zeros
   float scale;       // softmax scale (natural units)
   float scale_log2;  // scale * log2(e)
   int causal;
@@ -58,12 +59,15 @@ struct BwdParams {
 };
 
 // ------------------------------------------------------------------ prep
-// One row per D/8 threads (16-byte loads of O and dO); rows past N (padding)
-// get D = 0 and LSE2 = 0.
-template <int D>
+// One row per D/8 threads (16-byte loads of O and dO; a row has hd <= D
+// elements); rows past N (padding) get D = 0 and LSE2 = 0.
+// FULL: hd == D, the row length a compile-time constant.
+template <int D, bool FULL>
 __global__ void __launch_bounds__(PREP_THREADS)
     fattn_bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout, const float* __restrict__ lse,
-                          float* __restrict__ lse2, float* __restrict__ delta, int N, int N_pad, long long n_rows) {
+                          float* __restrict__ lse2, float* __restrict__ delta, int N, int N_pad, int hd_arg,
+                          long long n_rows) {
+  const int hd = FULL ? D : hd_arg;
   constexpr int TPR = D / 8;  // threads per row
   const long long r = ((long long)blockIdx.x * PREP_THREADS + threadIdx.x) / TPR;
   const int part = threadIdx.x % TPR;
@@ -71,8 +75,8 @@ __global__ void __launch_bounds__(PREP_THREADS)
   const long long bh = r / N_pad;
   const int i = (int)(r % N_pad);
   const bool live = r < n_rows && i < N;
-  if (live) {
-    const size_t at = ((size_t)bh * (size_t)N + (size_t)i) * (D / 8) + (size_t)part;
+  if (live && 8 * part < hd) {
+    const size_t at = ((size_t)bh * (size_t)N + (size_t)i) * (size_t)(hd / 8) + (size_t)part;
     const uint4 a = __ldg(o + at), g = __ldg(dout + at);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
@@ -157,11 +161,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // Rows [key0, key0 + 128) of an accumulator in TMEM -> bf16 rows of `out`
-// ([B*H, N, D]), times `mul`; rows at or past N are skipped.
+// ([B*H, N, hd]: the first hd of the D accumulator columns), times `mul`;
+// rows at or past N are skipped.
 template <int D>
 __device__ __forceinline__ void store_acc_rows(uint32_t t_addr, float mul, __nv_bfloat16* out, size_t row_flat,
-                                               bool row_ok) {
-  uint4* dst = reinterpret_cast<uint4*>(out + row_flat * D);
+                                               bool row_ok, int hd) {
+  uint4* dst = reinterpret_cast<uint4*>(out + row_flat * hd);
 #pragma unroll
   for (int hcol = 0; hcol < D / 64; ++hcol) {
     uint32_t av[64];
@@ -172,17 +177,20 @@ __device__ __forceinline__ void store_acc_rows(uint32_t t_addr, float mul, __nv_
     for (int x = 0; x < 32; ++x) ob[x] = pack_bf16x2(__uint_as_float(av[2 * x]) * mul, __uint_as_float(av[2 * x + 1]) * mul);
     if (row_ok) {
 #pragma unroll
-      for (int x = 0; x < 8; ++x) dst[8 * hcol + x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
+      for (int x = 0; x < 8; ++x)
+        if (64 * hcol + 8 * x < hd)
+          dst[8 * hcol + x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
     }
   }
 }
 
 template <int D>
-__device__ __forceinline__ void store_zero_rows(__nv_bfloat16* out, size_t row_flat, bool row_ok) {
+__device__ __forceinline__ void store_zero_rows(__nv_bfloat16* out, size_t row_flat, bool row_ok, int hd) {
   if (!row_ok) return;
-  uint4* dst = reinterpret_cast<uint4*>(out + row_flat * D);
+  uint4* dst = reinterpret_cast<uint4*>(out + row_flat * hd);
 #pragma unroll
-  for (int x = 0; x < D / 8; ++x) dst[x] = make_uint4(0, 0, 0, 0);
+  for (int x = 0; x < D / 8; ++x)
+    if (8 * x < hd) dst[x] = make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ int clamp_kl(const BwdParams& p, int b) {
@@ -353,8 +361,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const size_t row_flat = (size_t)bh * (size_t)p.N + (size_t)key;
     const bool row_ok = key < p.N;
     if (n_q == 0) {
-      store_zero_rows<D>(p.dv, row_flat, row_ok);
-      store_zero_rows<D>(p.dk, row_flat, row_ok);
+      store_zero_rows<D>(p.dv, row_flat, row_ok, p.hd);
+      store_zero_rows<D>(p.dk, row_flat, row_ok, p.hd);
     } else {
       const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
       const uint32_t s_addr = tmem + lane_off + BT_S;
@@ -436,8 +444,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        store_acc_rows<D>(tmem + lane_off + BT_ACC0, 1.0f, p.dv, row_flat, row_ok);
-        store_acc_rows<D>(tmem + lane_off + BT_ACC0 + D, p.scale, p.dk, row_flat, row_ok);
+        store_acc_rows<D>(tmem + lane_off + BT_ACC0, 1.0f, p.dv, row_flat, row_ok, p.hd);
+        store_acc_rows<D>(tmem + lane_off + BT_ACC0 + D, p.scale, p.dk, row_flat, row_ok, p.hd);
       }
     }
   }
@@ -657,7 +665,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const size_t row_flat = (size_t)bh * (size_t)p.N + (size_t)query;
     const bool row_ok = query < p.N;
     if (n_k == 0) {
-      store_zero_rows<D>(p.dq, row_flat, row_ok);
+      store_zero_rows<D>(p.dq, row_flat, row_ok, p.hd);
     } else {
       const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
       const uint32_t dp_addr = tmem + lane_off + BQ_DP;
@@ -717,7 +725,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        store_acc_rows<D>(tmem + lane_off + BQ_DQ, p.scale, p.dq, row_flat, row_ok);
+        store_acc_rows<D>(tmem + lane_off + BQ_DQ, p.scale, p.dq, row_flat, row_ok, p.hd);
       }
     }
   }

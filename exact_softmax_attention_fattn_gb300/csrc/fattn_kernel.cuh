@@ -81,6 +81,8 @@ struct Params {
   const uint8_t* v_mode;   // [B*H, mode_stride]: storage type of each V tile (VMODE_*)
   int* err;                // int[4]
   int B, H, N;
+  int hd;            // head dim of the tensors (a multiple of 8, <= D): rows are hd elements long;
+                     // the kernel computes D columns, the tensor maps read the rest as zeros
   float scale;       // softmax scale (natural units), >= 0
   float scale_log2;  // scale * log2(e)
   int causal;
@@ -96,7 +98,7 @@ struct Params {
 
 template <int D>
 struct Cfg {
-  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static_assert(D == 64 || D == 128, "head-dim bucket 64 or 128");
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t TILE_BYTES = BM * D * 2;  // one Q, K or V tile (BN == BM)
   static constexpr int STAGES = D == 128 ? 5 : 8;
@@ -343,11 +345,14 @@ __device__ __forceinline__ void static_for(F&& f) {
 // ------------------------------------------------------------------ the kernel
 // SPLIT: the split-KV instantiation (p.n_splits > 1: partial outputs in fp32
 // for the combine kernel); without it the kernel writes O and LSE itself.
-template <int D, bool SPLIT>
+// FULL: the head dim is D (rows of the output a compile-time length);
+// otherwise p.hd < D.
+template <int D, bool SPLIT, bool FULL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const Params p) {
   using C = Cfg<D>;
+  const int hd = FULL ? D : p.hd;  // output row length
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -654,9 +659,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if constexpr (SPLIT) continue;
         // no visible key at all: O = 0, LSE = -inf
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
+          uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * hd);
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < D / 8; ++i)
+            if (8 * i < hd) dst[i] = make_uint4(0, 0, 0, 0);
           p.lse[row_flat] = -INFINITY;
         }
         continue;
@@ -834,18 +840,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(bar_o_empty);
           }
           if (row_ok) {
-            float4* dstf = reinterpret_cast<float4*>(p.o_part + orow * D) + 16 * hcol;
+            float4* dstf = reinterpret_cast<float4*>(p.o_part + orow * hd) + 16 * hcol;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              dstf[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l, __uint_as_float(ov[4 * i + 1]) * inv_l,
-                                    __uint_as_float(ov[4 * i + 2]) * inv_l, __uint_as_float(ov[4 * i + 3]) * inv_l);
+              if (64 * hcol + 4 * i < hd)
+                dstf[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l, __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                      __uint_as_float(ov[4 * i + 2]) * inv_l, __uint_as_float(ov[4 * i + 3]) * inv_l);
           }
         }
         if (row_ok) p.lse_part[orow] = (m_ref * c + __log2f(l)) * 0.69314718055994531f;  // l > 0 here
       } else {
         // read O 64 columns at a time, pack to bf16 and store each half; O is
         // handed back to the MMA issuer once both halves are in registers
-        uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * D);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * hd);
 #pragma unroll
         for (int hcol = 0; hcol < D / 64; ++hcol) {
           uint32_t ov[64];
@@ -862,7 +869,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+              if (64 * hcol + 8 * i < hd)
+                dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
           }
         }
         if (row_ok) {

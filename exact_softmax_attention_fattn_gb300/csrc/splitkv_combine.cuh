@@ -41,10 +41,10 @@ template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS)
     fattn_splitkv_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                                  __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                 const int32_t* __restrict__ key_len, int B, int H, int N, int causal,
+                                 const int32_t* __restrict__ key_len, int B, int H, int N, int hd, int causal,
                                  int n_splits) {
   constexpr int VPT = 4;            // float4 per thread and split
-  constexpr int TPR = D / (4 * VPT);  // threads per row
+  constexpr int TPR = D / (4 * VPT);  // threads per row (rows of hd <= D columns)
   constexpr int ROWS = COMBINE_THREADS / TPR;
   const int row = blockIdx.x * ROWS + threadIdx.x / TPR;  // grid: (row blocks, heads)
   const int c4 = threadIdx.x % TPR;                       // float4 columns c4 + TPR * i, i < VPT
@@ -58,10 +58,11 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     const int n_blk = max(combine_tiles_of(blk0, N, kl, causal), combine_tiles_of(blk0 + 128, N, kl, causal));
     const int n_t = combine_tiles_of(row / 128 * 128, N, kl, causal);
     const size_t rg = (size_t)bh * N + row;
-    uint2* dst = reinterpret_cast<uint2*>(o + rg * D) + c4;
+    uint2* dst = reinterpret_cast<uint2*>(o + rg * hd) + c4;
     if (n_t == 0) {
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) dst[TPR * i] = make_uint2(0u, 0u);
+      for (int i = 0; i < VPT; ++i)
+        if (4 * (c4 + TPR * i) < hd) dst[TPR * i] = make_uint2(0u, 0u);
       if (c4 == 0) lse[rg] = -INFINITY;
       continue;
     }
@@ -80,10 +81,11 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
       const int j1 = (s + 1) * n_blk / n_splits;
       if (j1 > j0) {
         const float ls = lse_part[s * stride + rg];
-        const float4* src = reinterpret_cast<const float4*>(o_part + (s * stride + rg) * D) + c4;
+        const float4* src = reinterpret_cast<const float4*>(o_part + (s * stride + rg) * hd) + c4;
         float4 v[VPT];
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) v[i] = src[TPR * i];
+        for (int i = 0; i < VPT; ++i)
+          v[i] = 4 * (c4 + TPR * i) < hd ? src[TPR * i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         const float mn = fmaxf(m, ls);
         const float r = expf(m - mn);  // 0 for the first split (m = -inf)
         const float w = expf(ls - mn);
@@ -104,7 +106,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     for (int i = 0; i < VPT; ++i) {
       const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
       const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
-      dst[TPR * i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      if (4 * (c4 + TPR * i) < hd)
+        dst[TPR * i] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
     }
     if (c4 == 0) lse[rg] = m + logf(sum);
   }

@@ -21,19 +21,22 @@ namespace fattn {
 
 constexpr int PREPASS_THREADS = 256;
 
-template <int D>
+// FULL: rows are exactly D elements long (hd == D), with the row length a
+// compile-time constant; otherwise hd (a multiple of 8, < D).
+template <int D, bool FULL>
 __global__ void __launch_bounds__(PREPASS_THREADS)
     fattn_v_prepass_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, uint8_t* __restrict__ mode, int N,
-                           int n_tiles, int mode_stride) {
+                           int hd_arg, int n_tiles, int mode_stride) {
+  const int hd = FULL ? D : hd_arg;
   constexpr int VEC = 8;                                  // bf16 per 16-byte vector
-  constexpr int PER = BN * D / VEC / PREPASS_THREADS;     // vectors per thread
+  constexpr int PER = BN * D / VEC / PREPASS_THREADS;     // vectors per thread (rows of up to D elements)
   const long long tile_id = blockIdx.x;
   const int tile = (int)(tile_id % n_tiles);
   const long long bh = tile_id / n_tiles;
   const int row0 = tile * BN;
   const int rows = min(BN, N - row0);
-  const int nvec = rows * D / VEC;
-  const size_t base = ((size_t)bh * (size_t)N + (size_t)row0) * (D / VEC);
+  const int nvec = rows * hd / VEC;  // rows are hd (a multiple of 8) elements long
+  const size_t base = ((size_t)bh * (size_t)N + (size_t)row0) * (size_t)(hd / VEC);
 
   uint4 buf[PER];
   float mx = 0.0f;

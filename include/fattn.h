@@ -56,7 +56,10 @@ typedef enum {
  *   lse      device pointer, fp32, [B, H, N] contiguous, written (natural log).
  *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 0.
  *            If B*H*N == 0 the call does nothing and returns FATTN_OK.
- *   d        head dim: 64 or 128 (others return FATTN_ERR_UNSUPPORTED).
+ *   d        head dim: a multiple of 8 from 8 to 128 (others return
+ *            FATTN_ERR_UNSUPPORTED).  d <= 64 runs in the 64-column kernel,
+ *            larger d in the 128-column one; the columns past d are read as
+ *            zeros and never stored, so rows stay d elements long.
  *   scale    softmax scale applied to Q K^T before the mask; finite and >= 0
  *            (usually 1/sqrt(d)).
  *   causal   nonzero: key j is visible to query i only if j <= i.
@@ -90,8 +93,8 @@ typedef enum {
  *
  * Returns FATTN_OK, FATTN_ERR_INVALID_ARG (null pointer with B*H*N > 0,
  * negative size, misaligned pointer, host pointer, non-finite or negative
- * scale, sizes beyond int32 index space), FATTN_ERR_UNSUPPORTED (d not 64 or
- * 128) or FATTN_ERR_CUDA (launch failed; no kernel ran).  Argument errors
+ * scale, sizes beyond int32 index space), FATTN_ERR_UNSUPPORTED (d not a
+ * multiple of 8 in [8, 128]) or FATTN_ERR_CUDA (launch failed; no kernel ran).  Argument errors
  * are detected before anything is enqueued.
  */
 FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -122,8 +125,8 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
  * `stream` (per-row D and LSE in base 2) and returns it in stream order;
  * it enqueues three kernels on `stream` and returns without synchronising.
  *
- * Returns FATTN_OK, FATTN_ERR_INVALID_ARG, FATTN_ERR_UNSUPPORTED (d not in
- * {64, 128}) or FATTN_ERR_CUDA, with argument errors detected before anything
+ * Returns FATTN_OK, FATTN_ERR_INVALID_ARG, FATTN_ERR_UNSUPPORTED (d not a
+ * multiple of 8 in [8, 128]) or FATTN_ERR_CUDA, with argument errors detected before anything
  * is enqueued; time-outs of the kernels' bounded waits are reported by
  * fattn_last_error().
  */

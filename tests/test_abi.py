@@ -85,9 +85,16 @@ def test_null_pointer(lib, which):
     assert call(**{which: 0}) == binding.FATTN_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d", [0, 16, 32, 96, 127, 256])
+@pytest.mark.parametrize("d", [-8, 0, 4, 12, 100, 127, 136, 256])
 def test_unsupported_head_dim(lib, d):
+    """Head dims run: multiples of 8 from 8 to 128; others are refused before the device."""
     assert call(d=d) == binding.FATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d", [8, 32, 96, 120])
+def test_supported_head_dim_reaches_pointer_checks(lib, d):
+    """A supported head dim passes the head-dim check: the fake (host) pointers then fail."""
+    assert call(d=d) == binding.FATTN_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("which", ["q", "k", "v", "o"])
@@ -128,7 +135,8 @@ def test_backward_argument_checks(lib):
     for name in ("q", "k", "v", "o", "dout", "dq", "dk", "dv"):
         assert bcall(**{name: FAKE + 8}) == binding.FATTN_ERR_INVALID_ARG, name
     assert bcall(lse=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
-    assert bcall(d=96) == binding.FATTN_ERR_UNSUPPORTED
+    assert bcall(d=100) == binding.FATTN_ERR_UNSUPPORTED
+    assert bcall(d=136) == binding.FATTN_ERR_UNSUPPORTED
     buf = np.zeros(128 * 64 * 4, dtype=np.uint8)
     addr = buf.ctypes.data + (-buf.ctypes.data) % 16
     host = {n: addr for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")}
@@ -171,6 +179,6 @@ def test_splitkv_argument_checks(lib):
 
     assert callk(-1) == binding.FATTN_ERR_INVALID_ARG
     assert callk(2, B=0) == binding.FATTN_OK
-    assert callk(2, d=96) == binding.FATTN_ERR_UNSUPPORTED
+    assert callk(2, d=100) == binding.FATTN_ERR_UNSUPPORTED
     assert callk(2, scale=float("nan")) == binding.FATTN_ERR_INVALID_ARG
     assert callk(0, N=-1) == binding.FATTN_ERR_INVALID_ARG
