@@ -13,6 +13,7 @@
 
 #include "../../include/fattn.h"
 #include "fattn_bwd.cuh"
+#include "fattn_d256.cuh"
 #include "fattn_kernel.cuh"
 #include "splitkv_combine.cuh"
 #include "v_prepass.cuh"
@@ -69,6 +70,14 @@ int configure_fwd_kernel() {
   return FATTN_OK;
 }
 
+template <bool FULL>
+int configure_d256_kernel() {
+  return cudaFuncSetAttribute(fattn::fattn_fwd_d256_kernel<FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)fattn::D256Cfg::SMEM_BYTES) == cudaSuccess
+             ? FATTN_OK
+             : FATTN_ERR_CUDA;
+}
+
 template <int D>
 int configure_kernel() {
   int rc = configure_fwd_kernel<D, false, true>();
@@ -117,6 +126,8 @@ int device_state(int dev, DeviceState** out) {
     if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FATTN_ERR_CUDA;
     rc = configure_kernel<64>();
     if (rc == FATTN_OK) rc = configure_kernel<128>();
+    if (rc == FATTN_OK) rc = configure_d256_kernel<true>();
+    if (rc == FATTN_OK) rc = configure_d256_kernel<false>();
     if (rc != FATTN_OK) return rc;
     if (make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
     if (cudaMalloc(&s.err, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
@@ -138,13 +149,14 @@ bool is_device_pointer(const void* ptr) {
 }
 
 // [B*H, N, d] 16-bit elements viewed as a 3-D tensor: x = head dim (innermost),
-// y = row, z = batch*head.  Boxes of 64 x 128 x 1 with 128-byte swizzle; rows
-// past N and columns past d (head dims below the kernel's 64 or 128) read as
-// zero.
-int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType type) {
+// y = row, z = batch*head.  Boxes of 64 x box_rows x 1 with 128-byte swizzle;
+// rows past N and columns past d (head dims below the kernel's column count)
+// read as zero.
+int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType type,
+               unsigned box_rows = 128u) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2ull, (cuuint64_t)N * (cuuint64_t)d * 2ull};
-  cuuint32_t box[3] = {64u, 128u, 1u};
+  cuuint32_t box[3] = {64u, box_rows, 1u};
   cuuint32_t elem[3] = {1u, 1u, 1u};
   CUresult r = g_encode(map, type, 3, const_cast<void*>(ptr), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -155,9 +167,10 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Head dims the kernels run: multiples of 8 (rows of 16-byte vectors, TMA
-// strides in 16-byte units) up to 128, computed in the 64- or 128-column
-// instantiation with the columns past d read as zeros by the tensor maps.
-bool head_dim_supported(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+// strides in 16-byte units), computed in the 64-, 128- or 256-column kernel
+// with the columns past d read as zeros by the tensor maps.  The forward runs
+// up to 256, the backward up to 128.
+bool head_dim_supported(int d, int max_d = 256) { return d >= 8 && d <= max_d && d % 8 == 0; }
 
 // Scratch of one call: V in its per-tile storage type, then one mode byte per
 // tile, each head's row of modes padded to a multiple of 8 bytes; with
@@ -302,6 +315,39 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
   return FATTN_OK;
 }
 
+// Head dims 136..256: V pre-pass and the one-query-tile kernel (no split-KV);
+// `scratch` must hold scratch_bytes(..., 1).
+int enqueue_d256(const void* q, const void* k, const void* v, fattn::Params p, void* scratch, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  uint8_t* v16 = reinterpret_cast<uint8_t*>(scratch);
+  uint8_t* modes = v16 + round_up((size_t)BH * (size_t)p.N * (size_t)p.hd * 2u, 256);
+  p.v_mode = modes;
+  CUtensorMap mq, mk, mv;
+  if (encode_map(&mq, q, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128u) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (unsigned)fattn::D256_BN) != FATTN_OK ||
+      encode_map(&mv, v16, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (unsigned)fattn::D256_BN) != FATTN_OK)
+    return FATTN_ERR_CUDA;
+  const long long prepass_blocks = (long long)BH * p.n_kv_tiles;
+  const bool full = p.hd == fattn::D256;
+  if (full)
+    fattn::fattn_v_prepass_kernel<256, true><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
+        p.mode_stride);
+  else
+    fattn::fattn_v_prepass_kernel<256, false><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
+        p.mode_stride);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  const long long ctas = (long long)BH * ((p.N + fattn::BM - 1) / fattn::BM);
+  if (ctas > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  constexpr uint32_t smem = fattn::D256Cfg::SMEM_BYTES;
+  if (full)
+    fattn::fattn_fwd_d256_kernel<true><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+  else
+    fattn::fattn_fwd_d256_kernel<false><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 }  // namespace
@@ -357,7 +403,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.causal = causal ? 1 : 0;
   p.n_qblocks = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
   p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
-  p.n_splits = plan_splits(B, H, N, p.causal, ds->num_sms, splits_requested);
+  if (d > 128 && splits_requested > 1) return FATTN_ERR_UNSUPPORTED;  // no split-KV above 128 columns
+  p.n_splits = d > 128 ? 1 : plan_splits(B, H, N, p.causal, ds->num_sms, splits_requested);
   const long long units = (long long)B * H * p.n_qblocks * p.n_splits;
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
@@ -376,7 +423,9 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     cudaGetLastError();
     return FATTN_ERR_CUDA;
   }
-  rc = d <= 64 ? enqueue<64>(q, k, v, p, scratch, grid, s) : enqueue<128>(q, k, v, p, scratch, grid, s);
+  rc = d <= 64    ? enqueue<64>(q, k, v, p, scratch, grid, s)
+       : d <= 128 ? enqueue<128>(q, k, v, p, scratch, grid, s)
+                  : enqueue_d256(q, k, v, p, scratch, s);
   if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }
@@ -448,7 +497,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
-  if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d, 128)) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   const void* ptrs16[8] = {q, k, v, o, dout, dq, dk, dv};
   for (const void* ptr : ptrs16)
@@ -562,6 +611,8 @@ int noalloc_state(int dev, NoAllocState** out) {
     if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FATTN_ERR_CUDA;
     int rc = configure_kernel<64>();
     if (rc == FATTN_OK) rc = configure_kernel<128>();
+    if (rc == FATTN_OK) rc = configure_d256_kernel<true>();
+    if (rc == FATTN_OK) rc = configure_d256_kernel<false>();
     if (rc != FATTN_OK) return rc;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
@@ -630,5 +681,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the error word must start at zero for this call; the V copy and modes are fully rewritten
   if (cudaMemsetAsync(p.err, 0, 4 * sizeof(int), s) != cudaSuccess) return FATTN_ERR_CUDA;
-  return d <= 64 ? enqueue<64>(q, k, v, p, ns->scratch, grid, s) : enqueue<128>(q, k, v, p, ns->scratch, grid, s);
+  return d <= 64    ? enqueue<64>(q, k, v, p, ns->scratch, grid, s)
+         : d <= 128 ? enqueue<128>(q, k, v, p, ns->scratch, grid, s)
+                    : enqueue_d256(q, k, v, p, ns->scratch, s);
 }

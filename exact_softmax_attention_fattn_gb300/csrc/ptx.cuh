@@ -174,6 +174,22 @@ __device__ __forceinline__ void mma_ss_w_off(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// Same, with the A and B descriptors advanced by different compile-time
+// offsets (operand tiles whose panels differ in size).
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void mma_ss_w_off2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b64 ad, bd;\n\t"
+      "add.s64 ad, %1, %5;\n\t"
+      "add.s64 bd, %2, %6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+
 // TS form with the B descriptor advanced by OFF and the A TMEM column by ACOL.
 template <uint32_t OFF, uint32_t ACOL>
 __device__ __forceinline__ void mma_ts_w_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,

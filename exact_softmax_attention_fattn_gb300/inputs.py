@@ -142,9 +142,10 @@ def make_inputs(w: Workload) -> Inputs:
     return Inputs(w, q, k, v, key_len)
 
 
-# The five workloads the attention forward is measured and checked on, and a
-# long causal sequence with few heads: fewer blocks of 256 query rows (128)
-# than a GB300 has SMs (152), the shape split-KV is for.
+# The five workloads the attention forward is measured and checked on; a
+# long causal sequence with few heads (fewer blocks of 256 query rows, 128,
+# than a GB300 has SMs, 152: the shape split-KV is for); the headline shape
+# at two other head dims.
 WORKLOADS: dict[str, Workload] = {
     "b1h1n128d64": Workload("b1h1n128d64", 1, 1, 128, 64, False, 0),
     "b1h1n128d64_causal": Workload("b1h1n128d64_causal", 1, 1, 128, 64, True, 0),
@@ -156,6 +157,10 @@ WORKLOADS: dict[str, Workload] = {
         qk_sigma=2.0, key_len_range=(1024, 2048),
     ),
     "b1h2n16384d128_causal": Workload("b1h2n16384d128_causal", 1, 2, 16384, 128, True, 5),
+    # the headline shape at head dims outside {64, 128}: 96 (the 128-column
+    # kernel with zero columns) and 256 (the one-query-tile kernel)
+    "b2h16n4096d96_causal": Workload("b2h16n4096d96_causal", 2, 16, 4096, 96, True, 6),
+    "b2h16n4096d256_causal": Workload("b2h16n4096d256_causal", 2, 16, 4096, 256, True, 7),
 }
 
 HEADLINE = "b2h16n4096d128_causal"

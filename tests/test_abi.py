@@ -85,13 +85,13 @@ def test_null_pointer(lib, which):
     assert call(**{which: 0}) == binding.FATTN_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d", [-8, 0, 4, 12, 100, 127, 136, 256])
+@pytest.mark.parametrize("d", [-8, 0, 4, 12, 100, 127, 260, 264, 512])
 def test_unsupported_head_dim(lib, d):
-    """Head dims run: multiples of 8 from 8 to 128; others are refused before the device."""
+    """Head dims run by the forward: multiples of 8 from 8 to 256; others are refused before the device."""
     assert call(d=d) == binding.FATTN_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("d", [8, 32, 96, 120])
+@pytest.mark.parametrize("d", [8, 32, 96, 120, 136, 192, 256])
 def test_supported_head_dim_reaches_pointer_checks(lib, d):
     """A supported head dim passes the head-dim check: the fake (host) pointers then fail."""
     assert call(d=d) == binding.FATTN_ERR_INVALID_ARG
@@ -136,7 +136,8 @@ def test_backward_argument_checks(lib):
         assert bcall(**{name: FAKE + 8}) == binding.FATTN_ERR_INVALID_ARG, name
     assert bcall(lse=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
     assert bcall(d=100) == binding.FATTN_ERR_UNSUPPORTED
-    assert bcall(d=136) == binding.FATTN_ERR_UNSUPPORTED
+    assert bcall(d=136) == binding.FATTN_ERR_UNSUPPORTED  # the backward runs head dims up to 128
+    assert bcall(d=256) == binding.FATTN_ERR_UNSUPPORTED
     buf = np.zeros(128 * 64 * 4, dtype=np.uint8)
     addr = buf.ctypes.data + (-buf.ctypes.data) % 16
     host = {n: addr for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")}

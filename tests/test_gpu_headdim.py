@@ -1,10 +1,11 @@
 """Head dims other than 64 and 128 against the fp64 oracle.
 
-A head dim d (a multiple of 8, 8..128) runs in the 64- or 128-column
-kernels with the columns past d read as zeros by the tensor maps: they add
-nothing to Q K^T, give zero output columns that are never stored, and the
-rows in memory stay d elements long.  Forward (unsplit and split-KV) at the
-forward's bars, backward at the derived gradient bar, with poisoned guard
+A head dim d (a multiple of 8) runs in the 64- or 128-column kernels (d <=
+128) or the one-query-tile 256-column kernel (136..256), with the columns
+past d read as zeros by the tensor maps: they add nothing to Q K^T, give
+zero output columns that are never stored, and the rows in memory stay d
+elements long.  Forward (unsplit and, up to 128, split-KV) at the forward's
+bars, backward (up to 128) at the derived gradient bar, with poisoned guard
 bands around the outputs.
 """
 from __future__ import annotations
@@ -76,3 +77,56 @@ def test_backward_head_dims(cuda_device, d, causal):
     ours = guarded_backward(x, g, cuda_device, causal, scale)
     ref = oracle.backward(x.q, x.k, x.v, g, scale, causal)
     check_grads(ours, ref, f"backward d={d} causal={causal}")
+
+
+LARGE = [136, 192, 256]
+
+
+@pytest.mark.parametrize("d", LARGE)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 129, 300])
+def test_forward_large_head_dims(cuda_device, d, causal, N):
+    """The 64-key tiles of the 256-column kernel: N around one and two key tiles."""
+    x = make_inputs(Workload("hd_large", 2, 2, N, d, causal, 800 + d + N))
+    o_g, l_g = run_gpu(x, cuda_device)
+    o_r, l_r = oracle.forward(x.q, x.k, x.v, x.w.softmax_scale, causal)
+    compare(o_g, l_g, o_r, l_r, f"d={d} N={N} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_d256_key_padding_peaky(cuda_device, causal):
+    """Key lengths {0, 1, 65, 700} (a fully masked batch entry) with Q, K ~
+    N(0, 2^2): the rescale of the 256-column O runs."""
+    x = make_inputs(Workload("hd256_kl", 4, 2, 700, 256, causal, 901, qk_sigma=2.0))
+    kl = [0, 1, 65, 700]
+    o_g, l_g = run_gpu(x, cuda_device, key_len=kl)
+    o_r, l_r = oracle.forward(x.q, x.k, x.v, x.w.softmax_scale, causal, key_len=kl)
+    compare(o_g, l_g, o_r, l_r, f"d=256 key_len causal={causal}")
+
+
+def test_forward_d256_long(cuda_device):
+    """B1 H4 N4096 d256 causal: many CTAs and key tiles, sampled heads in full."""
+    x = make_inputs(Workload("hd256_long", 1, 4, 4096, 256, True, 902))
+    o_g, l_g = run_gpu(x, cuda_device)
+    rows = np.concatenate([h * 4096 + np.arange(4096) for h in (0, 3)]).astype(np.int64)
+    o_r, l_r = oracle.forward(x.q, x.k, x.v, x.w.softmax_scale, True, rows=rows)
+    compare(o_g.reshape(-1, 256)[rows], l_g.reshape(-1)[rows], o_r, l_r, "d=256 N=4096 causal")
+
+
+def test_large_head_dims_refuse_split_and_backward(cuda_device):
+    import torch
+
+    from exact_softmax_attention_fattn_gb300 import binding
+    from tests.gpu_helpers import bits_to_device
+
+    x = make_inputs(Workload("hd256_refuse", 1, 1, 256, 256, False, 903))
+    q, k, v = (bits_to_device(a, cuda_device) for a in (x.q, x.k, x.v))
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 256), dtype=torch.float32, device=cuda_device)
+    with pytest.raises(binding.FattnError) as e:
+        binding.forward_into(q, k, v, o, lse, n_splits=2)
+    assert e.value.status == binding.FATTN_ERR_UNSUPPORTED
+    binding.forward_into(q, k, v, o, lse, n_splits=1)  # one split is the plain forward
+    with pytest.raises(binding.FattnError) as e:
+        binding.backward(q, k, v, o, lse, q)
+    assert e.value.status == binding.FATTN_ERR_UNSUPPORTED
