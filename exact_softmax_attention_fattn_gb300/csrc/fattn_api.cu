@@ -330,16 +330,20 @@ int enqueue_d256(const void* q, const void* k, const void* v, fattn::Params p, v
   const long long prepass_blocks = (long long)BH * p.n_kv_tiles;
   const bool full = p.hd == fattn::D256;
   if (full)
-    fattn::fattn_v_prepass_kernel<256, true><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+    fattn::fattn_v_prepass_kernel<256, true><<<(unsigned)prepass_blocks, fattn::prepass_threads<256>(), 0, stream>>>(
         reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
         p.mode_stride);
   else
-    fattn::fattn_v_prepass_kernel<256, false><<<(unsigned)prepass_blocks, fattn::PREPASS_THREADS, 0, stream>>>(
+    fattn::fattn_v_prepass_kernel<256, false><<<(unsigned)prepass_blocks, fattn::prepass_threads<256>(), 0, stream>>>(
         reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
         p.mode_stride);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   const long long ctas = (long long)BH * ((p.N + fattn::BM - 1) / fattn::BM);
   if (ctas > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+  // heads per group of the CTA order: the K and V of a group's heads (read by
+  // every CTA of the head) should stay in L2 while the group runs, ~48 MB
+  const double kv_head = 4.0 * (double)p.N * (double)p.hd;
+  p.head_group = (int)std::max(1.0, std::min((double)BH, (48.0 * 1024 * 1024) / kv_head));
   constexpr uint32_t smem = fattn::D256Cfg::SMEM_BYTES;
   if (full)
     fattn::fattn_fwd_d256_kernel<true><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
@@ -409,6 +413,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
   p.o_part = nullptr;
+  p.head_group = 1;
   p.lse_part = nullptr;
   p.mode_stride = (p.n_kv_tiles + 7) / 8 * 8;
   if ((long long)B * H * p.mode_stride > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
@@ -672,6 +677,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   p.n_units = (int)units;
   p.n_splits = 1;  // no split-KV here: its partials would not fit a fixed array
   p.o_part = nullptr;
+  p.head_group = 1;
   p.lse_part = nullptr;
   p.n_kv_tiles = n_kv_tiles;
   p.mode_stride = (n_kv_tiles + 7) / 8 * 8;

@@ -8,7 +8,8 @@
 // tile, and K/V tiles are 64 keys deep so that Q (64 KB) and two-slot K and V
 // rings (4 x 32 KB) fit in shared memory.
 //
-//   * one CTA per (batch*head, 128-row query tile), heaviest tiles first under
+//   * one CTA per (batch*head, 128-row query tile), in groups of heads whose
+//     K and V fit in L2 together, heaviest tiles of a group first under
 //     causal; 192 threads: warps 0-3 form the softmax group (one query row
 //     per thread, a TMEM lane each), warp 4 is the TMA producer, warp 5
 //     issues tcgen05.mma;
@@ -19,8 +20,9 @@
 //     softmax group has released P_j), S_j+2.  The softmax of tile j+1 runs
 //     while the tensor core computes P_j V_j and S_j+2;
 //   * a rescale of O (skipped while the running max has grown by less than
-//     2^8, as in the main kernel) waits for the previous P V product, which
-//     the issuer signals after every tile;
+//     2^8, as in the main kernel) first waits for the previous P V product,
+//     which the issuer signals after every tile; P is otherwise released
+//     without waiting for it;
 //   * head dims below 256 (multiples of 8) are read with zero columns past d
 //     by the tensor maps and stored d columns wide;
 //   * every wait is bounded; on time-out the kernel records the error word,
@@ -58,9 +60,12 @@ struct D256Cfg {
   static constexpr int B_V_FULL = B_K_EMPTY + SLOTS;  // [SLOTS]
   static constexpr int B_V_EMPTY = B_V_FULL + SLOTS;  // [SLOTS]
   static constexpr int B_S_FULL = B_V_EMPTY + SLOTS;  // [2]: one per S buffer
-  static constexpr int B_P_FULL = B_S_FULL + 2;       // softmax group released P_j (128 arrivals)
-  static constexpr int B_PV_DONE = B_P_FULL + 1;      // P_j V_j completed
-  static constexpr int B_DRAIN = B_PV_DONE + 1;
+  // softmax group released P_j (128 arrivals), one per S buffer: the group
+  // may release P_j+1 before the issuer has looked at P_j's barrier
+  static constexpr int B_P_FULL = B_S_FULL + 2;       // [2]
+  static constexpr int B_PV_DONE = B_P_FULL + 2;      // P_j V_j completed
+  static constexpr int B_O_FULL = B_PV_DONE + 1;      // the last P V completed (once)
+  static constexpr int B_DRAIN = B_O_FULL + 1;
   static constexpr int NUM_BARS = B_DRAIN + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16;
@@ -84,12 +89,18 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(base_ptr + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::MISC_OFF + 4);
 
-  // the unit: (bh, query tile), heaviest first under causal
+  // the unit: (bh, query tile).  CTAs run in groups of head_group heads (the
+  // last group may be smaller); within a group the latest query tiles (the
+  // heaviest under causal) of all its heads come first.
   const int BH = p.B * p.H;
   const int n_qt = (p.N + BM - 1) / BM;
   const int u = (int)blockIdx.x;
-  const int bh = u % BH;
-  const int it_rev = u / BH;
+  const int per_group = p.head_group * n_qt;
+  const int g0 = (u / per_group) * p.head_group;
+  const int gsz = min(p.head_group, BH - g0);
+  const int rem = u % per_group;
+  const int bh = g0 + rem % gsz;
+  const int it_rev = rem / gsz;
   const int it = p.causal ? n_qt - 1 - it_rev : it_rev;
   const int row0 = it * BM;
   int kl = p.key_len ? p.key_len[bh / p.H] : p.N;
@@ -109,7 +120,9 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_S_FULL + 1), 1);
     mbar_init(bar(C::B_P_FULL), BM);
+    mbar_init(bar(C::B_P_FULL + 1), BM);
     mbar_init(bar(C::B_PV_DONE), 1);
+    mbar_init(bar(C::B_O_FULL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -212,7 +225,7 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % C::SLOTS;
         const uint32_t idesc_pv = __ldg(modes + (j * D256_BN) / BN) == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
-        ok = wait_bar(waiter, bar(C::B_P_FULL), (uint32_t)j & 1u, C::B_P_FULL, u);
+        ok = wait_bar(waiter, bar(C::B_P_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u, C::B_P_FULL + (j & 1), u);
         if (ok) ok = wait_bar(waiter, bar(C::B_V_FULL + s), (uint32_t)(j / C::SLOTS) & 1u, C::B_V_FULL + s, u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -234,6 +247,7 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
           issue_s(j + 2);
         }
       }
+      if (ok) mma_commit_w(bar(C::B_O_FULL));
       if (issued_any) {
         mma_commit_w(bar(C::B_DRAIN));
         drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
@@ -269,14 +283,30 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
         tc_fence_after();
         const bool masked_tile = (j + 1) * D256_BN > min_lim;
         const int vis_n = lim - j * D256_BN;  // columns [0, vis_n) visible
-        uint32_t sr[64];
-        tmem_ld64(s_addr, sr);
-        tmem_ld_wait(sr);
-        float mx = -INFINITY;
+        // S row of this tile; its max from the TMEM load's max reduction when
+        // no column is masked, else over the visible columns (tree order)
+        float sr[64];
+        float mx;
+        if (!masked_tile) {
+          tmem_ld64_max(s_addr, sr, mx);
+          tmem_ld_wait(sr, mx);
+        } else {
+          {
+            uint32_t r32[64];
+            tmem_ld64(s_addr, r32);
+            tmem_ld_wait(r32);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float v = __uint_as_float(sr[i]);
-          mx = fmaxf(mx, (masked_tile && i >= vis_n) ? -INFINITY : v);
+            for (int i = 0; i < 64; ++i) sr[i] = i < vis_n ? __uint_as_float(r32[i]) : -INFINITY;
+          }
+          float m8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmax3(sr[i], sr[i + 8], sr[i + 16]);
+#pragma unroll
+          for (int i = 24; i < 64; i += 16) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], sr[i + k], i + 8 + k < 64 ? sr[i + 8 + k] : -INFINITY);
+          }
+          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         const float m_new = fmaxf(m_ref, mx);
         float alpha = 1.0f;
@@ -289,32 +319,45 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
           rescale = true;
         }
         const float mc = m_ref * c;
-        // p = 2^(s*c - m*c), masked entries exactly 0; l from the unrounded p;
-        // P rounded to the V tile's operand type
+        // p = 2^(s*c - m*c) (packed f32x2 FMA, then ex2), masked entries
+        // exactly 0; l from the unrounded p in four packed partial sums; P
+        // rounded to the V tile's operand type
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nmc2 = f2_pack(-mc, -mc);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[32];
-        float rs = 0.0f;
         const bool f16 = vmode == VMODE_F16;
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
-          float p0 = ex2(fmaf(__uint_as_float(sr[2 * q]), c, -mc));
-          float p1 = ex2(fmaf(__uint_as_float(sr[2 * q + 1]), c, -mc));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sr[2 * q], sr[2 * q + 1]), c2, nmc2), x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
           if (masked_tile) {
             p0 = 2 * q < vis_n ? p0 : 0.0f;
             p1 = 2 * q + 1 < vis_n ? p1 : 0.0f;
           }
-          rs += p0 + p1;
+          acc[q % 4] = f2_add(acc[q % 4], f2_pack(p0, p1));
           pk[q] = f16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
+        float a0, a1, a2, a3, a4, a5, a6, a7;
+        f2_unpack(acc[0], a0, a1);
+        f2_unpack(acc[1], a2, a3);
+        f2_unpack(acc[2], a4, a5);
+        f2_unpack(acc[3], a6, a7);
+        const float rs = ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
         l = l * alpha + rs;
-        // O must not change under the previous P V product: wait for it
-        // (every tile, so the barrier's phases stay in step)
-        if (j > 0) {
-          ok = wait_bar(waiter, bar(C::B_PV_DONE), (uint32_t)(j - 1) & 1u, C::B_PV_DONE, u);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-        }
         if (__any_sync(0xffffffffu, rescale)) {
+          // O must not change under the previous P V product: wait for it.
+          // Waited only here and in the epilogue: when tile j's S has landed,
+          // P_j-2 V_j-2 has completed (S_j was issued after it) and P_j V_j
+          // cannot start before this P is released, so the barrier is at
+          // phase j-1 or j and the parity of phase j-1 names it exactly.
+          if (j > 0) {
+            ok = wait_bar(waiter, bar(C::B_PV_DONE), (uint32_t)(j - 1) & 1u, C::B_PV_DONE, u);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+          }
 #pragma unroll 1
           for (int cc = 0; cc < D256 / 32; ++cc) {
             uint32_t r32[32];
@@ -328,11 +371,12 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
         tmem_st32(s_addr, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::B_P_FULL));
+        mbar_arrive(bar(C::B_P_FULL + (j & 1)));
       }
       if (ok) {
-        // epilogue: the last P V product, then O / l -> bf16, LSE = m*scale + ln(l)
-        ok = wait_bar(waiter, bar(C::B_PV_DONE), (uint32_t)(n - 1) & 1u, C::B_PV_DONE, u);
+        // epilogue: the last P V product (its own barrier: P V products may
+        // still be two deep here), then O / l -> bf16, LSE = m*scale + ln(l)
+        ok = wait_bar(waiter, bar(C::B_O_FULL), 0, C::B_O_FULL, u);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {

@@ -89,6 +89,7 @@ struct Params {
   int n_qblocks;  // ceil(N / 256)
   int n_units;    // B * H * n_qblocks * n_splits
   int n_splits;    // K/V splits per query block (1: no split, O and LSE written directly)
+  int head_group;  // one-query-tile kernel (head dims above 128): heads per group of its CTA order
   float* o_part;   // n_splits > 1: [n_splits, B*H, N, D] fp32 O / l of each split
   float* lse_part; // n_splits > 1: [n_splits, B*H, N] fp32 log-sum-exp of each split
   int n_kv_tiles; // ceil(N / 128)

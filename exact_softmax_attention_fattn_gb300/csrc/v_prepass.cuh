@@ -20,16 +20,20 @@
 namespace fattn {
 
 constexpr int PREPASS_THREADS = 256;
+// threads of one block: 8 vectors of 16 bytes per thread at every head-dim bucket
+template <int D>
+__host__ __device__ constexpr int prepass_threads() { return D > 128 ? 512 : PREPASS_THREADS; }
 
 // FULL: rows are exactly D elements long (hd == D), with the row length a
 // compile-time constant; otherwise hd (a multiple of 8, < D).
 template <int D, bool FULL>
-__global__ void __launch_bounds__(PREPASS_THREADS)
+__global__ void __launch_bounds__(prepass_threads<D>())
     fattn_v_prepass_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, uint8_t* __restrict__ mode, int N,
                            int hd_arg, int n_tiles, int mode_stride) {
   const int hd = FULL ? D : hd_arg;
   constexpr int VEC = 8;                                  // bf16 per 16-byte vector
-  constexpr int PER = BN * D / VEC / PREPASS_THREADS;     // vectors per thread (rows of up to D elements)
+  constexpr int T = prepass_threads<D>();
+  constexpr int PER = BN * D / VEC / T;  // vectors per thread (rows of up to D elements)
   const long long tile_id = blockIdx.x;
   const int tile = (int)(tile_id % n_tiles);
   const long long bh = tile_id / n_tiles;
@@ -42,7 +46,7 @@ __global__ void __launch_bounds__(PREPASS_THREADS)
   float mx = 0.0f;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int idx = threadIdx.x + i * PREPASS_THREADS;
+    const int idx = threadIdx.x + i * T;
     if (idx < nvec) {
       buf[i] = __ldg(v + base + idx);
       const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
@@ -53,19 +57,19 @@ __global__ void __launch_bounds__(PREPASS_THREADS)
       }
     }
   }
-  __shared__ float warp_max[PREPASS_THREADS / 32];
+  __shared__ float warp_max[T / 32];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (threadIdx.x % 32 == 0) warp_max[threadIdx.x / 32] = mx;
   __syncthreads();
   mx = warp_max[0];
 #pragma unroll
-  for (int i = 1; i < PREPASS_THREADS / 32; ++i) mx = fmaxf(mx, warp_max[i]);
+  for (int i = 1; i < T / 32; ++i) mx = fmaxf(mx, warp_max[i]);
   const bool to_f16 = mx >= 0.00390625f && mx <= 65504.0f;
 
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int idx = threadIdx.x + i * PREPASS_THREADS;
+    const int idx = threadIdx.x + i * T;
     if (idx < nvec) {
       uint4 o = buf[i];
       if (to_f16) {
