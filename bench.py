@@ -327,14 +327,14 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     if not args.no_e2e:
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         klh = None if x.key_len is None else torch.from_numpy(x.key_len)
+        # fattn_fwd_host through the public forward() (the library's own split-KV choice per chunk)
         for _ in range(2):
-            binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh, n_splits=args.splits)
+            binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh)
         n_e2e = max(3, min(args.steps, 10))
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(n_e2e):
-            oh, lh = binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh,
-                                     n_splits=args.splits)
+            oh, lh = binding.forward(qh, kh, vh, causal=w.causal, scale=w.softmax_scale, key_len=klh)
         torch.cuda.synchronize(dev)
         e2e_s = (time.perf_counter() - t0) / n_e2e
         h2d = 3 * q.numel() * 2 + (0 if klh is None else klh.numel() * 4)

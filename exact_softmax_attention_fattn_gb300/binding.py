@@ -22,8 +22,8 @@ FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
-EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_splitkv_plan", "fattn_bwd", "fattn_status_string",
-            "fattn_last_error", "fattn_version")
+EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_splitkv_plan", "fattn_bwd",
+            "fattn_status_string", "fattn_last_error", "fattn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +66,8 @@ def load_library():
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
             ]
+            lib.fattn_fwd_host.restype = ctypes.c_int
+            lib.fattn_fwd_host.argtypes = lib.fattn_fwd.argtypes
             lib.fattn_splitkv_plan.restype = ctypes.c_int
             lib.fattn_splitkv_plan.argtypes = [ctypes.c_int] * 6
             lib.fattn_bwd.restype = ctypes.c_int
@@ -95,6 +97,13 @@ def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int
                                         float(scale), int(bool(causal)), key_len_ptr, stream)
     return load_library().fattn_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                                             float(scale), int(bool(causal)), key_len_ptr, int(n_splits), stream)
+
+
+def fwd_host_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, d: int,
+                 scale: float, causal: bool, key_len_ptr: int | None, stream: int | None) -> int:
+    """fattn_fwd_host with raw HOST addresses; returns the status code."""
+    return load_library().fattn_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
+                                         float(scale), int(bool(causal)), key_len_ptr, stream)
 
 
 def splitkv_plan(B: int, H: int, N: int, causal: bool, num_sms: int, n_splits: int = 0) -> int:
@@ -208,23 +217,36 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=N
     """O, LSE = attention forward of bf16 [B, H, N, d] tensors.
 
     Device tensors: the kernel is enqueued on the current stream and the call
-    returns without synchronising.  Host tensors (pinned for speed): they are
-    copied to the current CUDA device, the kernel runs there, and O and LSE
-    are copied back (the call then synchronises).
+    returns without synchronising.  Host tensors (pinned for speed): one
+    fattn_fwd_host call on the current CUDA device (host <-> device copies
+    overlapped with the kernels, chunk by chunk) into pinned host O and LSE;
+    the call synchronises before returning them (n_splits must be None).
     `key_len` may be a tensor, a sequence of ints or None.
     """
     import torch
 
-    on_host = q.device.type == "cpu"
-    if on_host:
+    if q.device.type == "cpu":
         if not torch.cuda.is_available():
             raise FattnError(FATTN_ERR_CUDA, "no CUDA device")
+        if n_splits is not None:
+            raise ValueError("n_splits applies to device tensors only")
+        _check_qkv(q, k, v)
+        B, H, N, d = q.shape
+        kl_h = None if key_len is None else torch.as_tensor(key_len, dtype=torch.int32).cpu().contiguous()
+        if kl_h is not None and kl_h.shape != (B,):
+            raise ValueError("key_len must hold B values")
+        o_h = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        l_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
         dev = torch.device("cuda", torch.cuda.current_device())
-        qd = q.to(dev, non_blocking=True)
-        kd = k.to(dev, non_blocking=True)
-        vd = v.to(dev, non_blocking=True)
-    else:
-        dev, qd, kd, vd = q.device, q, k, v
+        stream = torch.cuda.current_stream(dev)
+        st = fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_h.data_ptr(), l_h.data_ptr(), B, H, N, d,
+                          1.0 / math.sqrt(d) if scale is None else scale, causal,
+                          None if kl_h is None else kl_h.data_ptr(), stream.cuda_stream)
+        if st != FATTN_OK:
+            raise FattnError(st, "fattn_fwd_host")
+        stream.synchronize()
+        return o_h, l_h
+    dev, qd, kd, vd = q.device, q, k, v
     _check_qkv(qd, kd, vd)
     kl = None
     if key_len is not None:
@@ -233,11 +255,4 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, key_len=N
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     forward_into(qd, kd, vd, o, lse, causal=causal, scale=scale, key_len=kl, n_splits=n_splits)
-    if on_host:
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        l_h.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
-        return o_h, l_h
     return o, lse

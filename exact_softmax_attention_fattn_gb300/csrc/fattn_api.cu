@@ -31,6 +31,8 @@ struct DeviceState {
   int num_sms = 0;
   int* err = nullptr;             // int[4] device workspace
   cudaMemPool_t pool = nullptr;   // private stream-ordered pool for per-call scratch
+  cudaStream_t copy_in = nullptr;   // host-buffer entry point: host -> device copies
+  cudaStream_t copy_out = nullptr;  // and device -> host copies
 };
 
 std::mutex g_mu;
@@ -131,6 +133,9 @@ int device_state(int dev, DeviceState** out) {
     if (rc != FATTN_OK) return rc;
     if (make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
     if (cudaMalloc(&s.err, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&s.copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&s.copy_out, cudaStreamNonBlocking) != cudaSuccess)
+      return FATTN_ERR_CUDA;
     if (cudaMemset(s.err, 0, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return FATTN_ERR_CUDA;
     s.ready = true;
@@ -371,8 +376,11 @@ extern "C" FATTN_API const char* fattn_status_string(int status) {
 
 namespace {
 
+// check_pointers = false: the caller owns the buffers (the host-buffer entry
+// point's chunks inside its pool allocation) and has validated the rest.
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-               float scale, int causal, const int32_t* key_len, int splits_requested, void* stream) {
+               float scale, int causal, const int32_t* key_len, int splits_requested, void* stream,
+               bool check_pointers = true) {
   // ---- synchronous argument checks: nothing is enqueued on failure
   if (B < 0 || H < 0 || N < 0 || splits_requested < 0) return FATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
@@ -383,8 +391,9 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       (key_len && !aligned(key_len, 4)))
     return FATTN_ERR_INVALID_ARG;
-  if (!is_device_pointer(q) || !is_device_pointer(k) || !is_device_pointer(v) || !is_device_pointer(o) ||
-      !is_device_pointer(lse) || (key_len && !is_device_pointer(key_len)))
+  if (check_pointers &&
+      (!is_device_pointer(q) || !is_device_pointer(k) || !is_device_pointer(v) || !is_device_pointer(o) ||
+       !is_device_pointer(lse) || (key_len && !is_device_pointer(key_len))))
     return FATTN_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -446,6 +455,134 @@ extern "C" FATTN_API int fattn_fwd_splitkv(const void* q, const void* k, const v
                                            int H, int N, int d, float scale, int causal, const int32_t* key_len,
                                            int n_splits, void* stream) {
   return fwd_common(q, k, v, o, lse, B, H, N, d, scale, causal, key_len, n_splits, stream);
+}
+
+// ------------------------------------------------------------------------
+// fattn_fwd_host: the forward on host buffers.  The problem is cut into a few
+// chunks (ranges of whole batch entries, or of heads within one entry, so
+// that each chunk has one key-length pointer); chunk i's inputs are copied
+// in on one stream while chunk i-1 computes on the caller's stream and chunk
+// i-2's outputs are copied out on a third.
+namespace {
+
+struct HostChunk {
+  int b0, nb;  // batch entries [b0, b0 + nb)
+  int h0, nh;  // heads [h0, h0 + nh) of each
+};
+
+std::vector<HostChunk> host_chunks(int B, int H, long long bytes) {
+  const int target = bytes < (16ll << 20) ? 1 : 8;  // small problems: one chunk
+  std::vector<HostChunk> c;
+  if (B >= target) {
+    for (int i = 0; i < target; ++i) {
+      const int b0 = (int)((long long)B * i / target), b1 = (int)((long long)B * (i + 1) / target);
+      if (b1 > b0) c.push_back({b0, b1 - b0, 0, H});
+    }
+  } else {
+    const int per_b = std::min(H, (target + B - 1) / B);
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < per_b; ++i) {
+        const int h0 = (int)((long long)H * i / per_b), h1 = (int)((long long)H * (i + 1) / per_b);
+        if (h1 > h0) c.push_back({b, 1, h0, h1 - h0});
+      }
+  }
+  return c;
+}
+
+}  // namespace
+
+extern "C" FATTN_API int fattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                        int H, int N, int d, float scale, int causal, const int32_t* key_len,
+                                        void* stream) {
+  if (B < 0 || H < 0 || N < 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
+  if (is_device_pointer(q) || is_device_pointer(k) || is_device_pointer(v) || is_device_pointer(o) ||
+      is_device_pointer(lse) || (key_len && is_device_pointer(key_len)))
+    return FATTN_ERR_INVALID_ARG;  // host buffers only (fattn_fwd takes device ones)
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  int rc = device_state(dev, &ds);
+  if (rc != FATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const size_t n_elem = (size_t)B * H * (size_t)N * (size_t)d;
+  const size_t t16 = round_up(n_elem * 2u, 256), t_lse = round_up((size_t)B * H * (size_t)N * 4u, 256);
+  void* buf = nullptr;
+  if (cudaMallocFromPoolAsync(&buf, 4 * t16 + t_lse + round_up((size_t)B * 4u, 256), ds->pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  uint8_t* base = reinterpret_cast<uint8_t*>(buf);
+  uint16_t* qd = reinterpret_cast<uint16_t*>(base);
+  uint16_t* kd = reinterpret_cast<uint16_t*>(base + t16);
+  uint16_t* vd = reinterpret_cast<uint16_t*>(base + 2 * t16);
+  uint16_t* od = reinterpret_cast<uint16_t*>(base + 3 * t16);
+  float* lsed = reinterpret_cast<float*>(base + 4 * t16);
+  int32_t* kld = reinterpret_cast<int32_t*>(base + 4 * t16 + t_lse);
+
+  const std::vector<HostChunk> chunks = host_chunks(B, H, (long long)(n_elem * 2u));
+  const int nc = (int)chunks.size();
+  std::vector<cudaEvent_t> ev(2 * nc + 2, nullptr);
+  for (auto& e : ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) rc = FATTN_ERR_CUDA;
+  cudaEvent_t ev_alloc = ev[2 * nc], ev_done = ev[2 * nc + 1];
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (rc == FATTN_OK && !(ok(cudaEventRecord(ev_alloc, s)) && ok(cudaStreamWaitEvent(ds->copy_in, ev_alloc, 0))))
+    rc = FATTN_ERR_CUDA;
+  if (rc == FATTN_OK && key_len &&
+      !ok(cudaMemcpyAsync(kld, key_len, (size_t)B * 4u, cudaMemcpyHostToDevice, ds->copy_in)))
+    rc = FATTN_ERR_CUDA;
+  const uint16_t* qh = reinterpret_cast<const uint16_t*>(q);
+  const uint16_t* kh = reinterpret_cast<const uint16_t*>(k);
+  const uint16_t* vh = reinterpret_cast<const uint16_t*>(v);
+  uint16_t* oh = reinterpret_cast<uint16_t*>(o);
+  auto rows_of = [&](const HostChunk& c) { return (size_t)c.nb * c.nh * (size_t)N; };
+  auto row0_of = [&](const HostChunk& c) { return ((size_t)c.b0 * H + c.h0) * (size_t)N; };
+  // inputs, chunk by chunk
+  for (int i = 0; rc == FATTN_OK && i < nc; ++i) {
+    const size_t e0 = row0_of(chunks[i]) * d, ne = rows_of(chunks[i]) * d;
+    if (!(ok(cudaMemcpyAsync(qd + e0, qh + e0, ne * 2u, cudaMemcpyHostToDevice, ds->copy_in)) &&
+          ok(cudaMemcpyAsync(kd + e0, kh + e0, ne * 2u, cudaMemcpyHostToDevice, ds->copy_in)) &&
+          ok(cudaMemcpyAsync(vd + e0, vh + e0, ne * 2u, cudaMemcpyHostToDevice, ds->copy_in)) &&
+          ok(cudaEventRecord(ev[i], ds->copy_in))))
+      rc = FATTN_ERR_CUDA;
+  }
+  // compute each chunk once its inputs are in, then copy its outputs out
+  for (int i = 0; rc == FATTN_OK && i < nc; ++i) {
+    const HostChunk& c = chunks[i];
+    const size_t r0 = row0_of(c), nr = rows_of(c);
+    if (!ok(cudaStreamWaitEvent(s, ev[i], 0))) {
+      rc = FATTN_ERR_CUDA;
+      break;
+    }
+    rc = fwd_common(qd + r0 * d, kd + r0 * d, vd + r0 * d, od + r0 * d, lsed + r0, c.nb, c.nh, N, d, scale, causal,
+                    key_len ? kld + c.b0 : nullptr, 0, stream, false);
+    if (rc != FATTN_OK) break;
+    if (!(ok(cudaEventRecord(ev[nc + i], s)) && ok(cudaStreamWaitEvent(ds->copy_out, ev[nc + i], 0)) &&
+          ok(cudaMemcpyAsync(oh + r0 * d, od + r0 * d, nr * d * 2u, cudaMemcpyDeviceToHost, ds->copy_out)) &&
+          ok(cudaMemcpyAsync(lse + r0, lsed + r0, nr * 4u, cudaMemcpyDeviceToHost, ds->copy_out))))
+      rc = FATTN_ERR_CUDA;
+  }
+  // join both copy streams back into the caller's stream, then release the buffers there
+  cudaEvent_t ev_in_done = ev[2 * nc];  // reused: the allocation event has been consumed
+  bool joined = ok(cudaEventRecord(ev_in_done, ds->copy_in)) && ok(cudaStreamWaitEvent(s, ev_in_done, 0)) &&
+                ok(cudaEventRecord(ev_done, ds->copy_out)) && ok(cudaStreamWaitEvent(s, ev_done, 0));
+  if (!joined) {
+    // cannot order the release after the copies: wait for them here instead
+    cudaStreamSynchronize(ds->copy_in);
+    cudaStreamSynchronize(ds->copy_out);
+    if (rc == FATTN_OK) rc = FATTN_ERR_CUDA;
+  }
+  if (cudaFreeAsync(buf, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
+  for (auto& e : ev)
+    if (e) cudaEventDestroy(e);
+  return rc;
 }
 
 extern "C" FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits) {

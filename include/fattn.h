@@ -157,6 +157,36 @@ FATTN_API int fattn_fwd_splitkv(const void* q, const void* k, const void* v, voi
                                 void* stream);
 
 /*
+ * fattn_fwd_host: fattn_fwd on HOST buffers, with the host <-> device copies
+ * overlapped with the computation.
+ *
+ *   q, k, v  host pointers, bf16 [B, H, N, d] (pinned memory lets the copies
+ *            run asynchronously; pageable memory works, with copies that
+ *            block the calling thread).
+ *   o, lse   host pointers, written: bf16 O [B, H, N, d] and fp32 LSE [B, H, N].
+ *   key_len  host pointer to int32[B] or NULL.
+ *   Other arguments as for fattn_fwd; head dims as for fattn_fwd.
+ *
+ * The call takes device buffers for Q, K, V, O, LSE and key_len from the
+ * library's pool, cuts the problem into up to eight chunks (ranges of whole
+ * batch entries, or of heads within one entry), and enqueues per chunk: the
+ * copies of its inputs on a library stream, fattn_fwd on `stream` once they
+ * have landed, and the copies of its outputs on a second library stream, so
+ * that copies in both directions overlap other chunks' kernels.  Both
+ * library streams are joined back into `stream` and the buffers are
+ * released there: o and lse hold the results once `stream` has reached this
+ * point (synchronise it before reading them).  Results are those of
+ * fattn_fwd on the same data (each chunk is a smaller fattn_fwd problem, so
+ * the library's split-KV choice may differ per chunk).
+ *
+ * Returns the codes of fattn_fwd; FATTN_ERR_INVALID_ARG also for a device
+ * pointer among the buffers.  Argument errors are detected before anything
+ * is enqueued.
+ */
+FATTN_API int fattn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                             int d, float scale, int causal, const int32_t* key_len, void* stream);
+
+/*
  * fattn_splitkv_plan: the split count the forward uses, computed on the host
  * alone (no GPU, no CUDA call).  n_splits as for fattn_fwd_splitkv: k > 0
  * returns min(k, ceil(N/128)); 0 returns the library's choice: 1 whenever

@@ -183,3 +183,17 @@ def test_splitkv_argument_checks(lib):
     assert callk(2, d=100) == binding.FATTN_ERR_UNSUPPORTED
     assert callk(2, scale=float("nan")) == binding.FATTN_ERR_INVALID_ARG
     assert callk(0, N=-1) == binding.FATTN_ERR_INVALID_ARG
+
+
+def hcall(B=1, H=1, N=128, d=64, scale=0.125, causal=0, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, kl=None):
+    return binding.fwd_host_raw(q, k, v, o, lse, B, H, N, d, scale, causal, kl, None)
+
+
+def test_host_entry_point_argument_checks(lib):
+    """fattn_fwd_host validates like fattn_fwd before touching the device."""
+    assert hcall(B=0) == binding.FATTN_OK
+    assert hcall(N=-1) == binding.FATTN_ERR_INVALID_ARG
+    assert hcall(scale=math.nan) == binding.FATTN_ERR_INVALID_ARG
+    assert hcall(d=100) == binding.FATTN_ERR_UNSUPPORTED
+    for name in ("q", "k", "v", "o", "lse"):
+        assert hcall(**{name: 0}) == binding.FATTN_ERR_INVALID_ARG, name
