@@ -24,13 +24,24 @@ CHILD = r"""
 import json, sys
 import numpy as np, torch
 sys.path.insert(0, sys.argv[1])
+case = sys.argv[2]
 from exact_softmax_attention_fattn_gb300 import binding
 from exact_softmax_attention_fattn_gb300.inputs import Workload, make_inputs
-x = make_inputs(Workload("to", 1, 4, 2048, 128, True, 50))
+# shapes whose waits run well past 1 us: the 256-column kernel, whose CTAs
+# each hold one query tile, gets a non-causal problem (every CTA 64 key tiles)
+shapes = {"fwd": (1, 4, 2048, 128, True), "split": (1, 2, 4096, 128, True), "d256": (1, 8, 4096, 256, False),
+          "bwd": (1, 2, 1024, 128, True)}
+B, H, N, d, causal = shapes[case]
+x = make_inputs(Workload("to", B, H, N, d, causal, 50))
 dev = torch.device("cuda:0")
 q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in (x.q, x.k, x.v))
-o = torch.empty_like(q); lse = torch.empty((1, 4, 2048), dtype=torch.float32, device=dev)
-binding.forward_into(q, k, v, o, lse, causal=True)
+o = torch.zeros_like(q); lse = torch.zeros((B, H, N), dtype=torch.float32, device=dev)
+if case == "bwd":
+    binding.last_error()                  # start clean
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    binding.backward_into(q, k, v, o, lse, q, dq, dk, dv, causal=causal)
+else:
+    binding.forward_into(q, k, v, o, lse, causal=causal, n_splits=4 if case == "split" else None)
 st, detail = binding.last_error()
 again, _ = binding.last_error()          # the flag is cleared once read
 a = torch.randn(512, 512, device=dev)
@@ -40,9 +51,15 @@ print(json.dumps({"status": st, "detail": detail, "again": again, "context_ok": 
 """
 
 
-def test_bounded_wait_times_out_and_reports(cuda_device):
+@pytest.mark.parametrize("case", ["fwd", "split", "d256", "bwd"])
+def test_bounded_wait_times_out_and_reports(cuda_device, case):
+    """Each kernel family (the forward, its split-KV instantiation, the
+    256-column forward, the backward's kernels) times out for real and
+    reports; the backward runs on zero O and LSE (values do not matter
+    here)."""
     env = dict(os.environ, FATTN_WAIT_LIMIT_US="1")
-    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, capture_output=True, text=True, timeout=300)
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT, case], env=env, capture_output=True, text=True,
+                       timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
     assert res["status"] == 4  # FATTN_ERR_TIMEOUT
