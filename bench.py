@@ -29,6 +29,11 @@ workload, in the same metric.
 forward's O and LSE, which are computed once before the timed region), with
 FLOPs counted as 2.5x the forward's (five GEMMs of the forward's size).
 
+roofline.achieved is the dominant kernel's rate on its own device time: the
+library records two CUDA events around it on its stream
+(fattn_set_kernel_events) -- the attention kernel of the forward, the dK/dV
+kernel of the backward -- while `value` covers the whole step.
+
 The forward splits each query block's key range (split-KV, with a combine
 kernel) when the library's plan says so -- on shapes with fewer blocks of 256
 query rows than SMs; --splits K forces K splits (1: none), and the split count
@@ -158,6 +163,18 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
                 "samples": len(sm), "power_w_max": float(max(power)) if power else None}
+
+
+def kernel_event_pairs(n: int, stream):
+    """n (start, stop) CUDA event pairs for fattn_set_kernel_events, recorded
+    once so that their CUDA events exist."""
+    import torch
+
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in pairs:
+        a.record(stream)
+        b.record(stream)
+    return pairs
 
 
 def warm_up(step, flush, warmup: int, sampler, dev, load_seconds: float = 0.5) -> int:
@@ -302,15 +319,18 @@ def our_arm(args, rank: int, world: int, local_rank: int):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kev = kernel_event_pairs(args.steps, stream)  # around the attention kernel, recorded by the library
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
+        binding.set_kernel_events(*kev[i])
         starts[i].record(stream)
         step()
         ends[i].record(stream)
+    binding.set_kernel_events(None, None)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     if world > 1:
@@ -320,6 +340,7 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     if st != binding.FATTN_OK:
         raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [a.elapsed_time(b) for a, b in kev]
     ms_per_step, value = aggregate_ranks(float(sum(kernel_ms)), flops, args.steps, world, dev)
 
     # end to end through the public API with host buffers
@@ -345,7 +366,9 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     if rank != 0:
         return
     peak, peak_kind, _ = measured_peaks()
-    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    # the dominant kernel (the attention kernel) on its own CUDA-event time
+    attn_mean_ms = float(np.mean(attn_ms))
+    achieved = flops / (attn_mean_ms * 1e-3) / 1e12
     traffic = ncu_traffic(args.workload)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -364,8 +387,10 @@ def our_arm(args, rank: int, world: int, local_rank: int):
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "traffic": traffic if n_splits == 1 else None},
-        "pct_of_bf16_peak": 100.0 * achieved / peak,
+                     "traffic": traffic if n_splits == 1 else None,
+                     "kernel": "attention kernel alone (V pre-pass and split-KV combine excluded)",
+                     "kernel_ms_mean": attn_mean_ms},
+        "pct_of_bf16_peak": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / peak,
         "clocks": clocks,
         "e2e": e2e,
         # V pre-pass + attention kernel per step, + the split-KV combine when split
@@ -415,13 +440,16 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
         raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kev = kernel_event_pairs(args.steps, stream)  # around the dK/dV kernel, recorded by the library
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
+        binding.set_kernel_events(*kev[i])
         starts[i].record(stream)
         step()
         ends[i].record(stream)
+    binding.set_kernel_events(None, None)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
@@ -429,6 +457,7 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
     if st != binding.FATTN_OK:
         raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
     kernel_ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    dkdv_ms = [a.elapsed_time(b) for a, b in kev]
     ms_per_step, value = aggregate_ranks(float(sum(kernel_ms)), flops, args.steps, world, dev)
 
     # end to end: the six inputs copied in from pinned host buffers, three gradients copied out
@@ -456,7 +485,9 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
     if rank != 0:
         return
     peak, peak_kind, _ = measured_peaks()
-    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    # the dominant kernel (dK/dV: S, dP, dV, dK = 4 of the forward's 2 GEMMs) on its own CUDA-event time
+    dkdv_mean_ms = float(np.mean(dkdv_ms))
+    achieved = (flops / 2.5 * 2.0) / (dkdv_mean_ms * 1e-3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         # the fp64 oracle backward on one head (about 2.5x the head's forward FLOPs)
@@ -476,8 +507,10 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
                    "causal": w.causal, "key_padding": x.key_len is not None, "flops_per_step": flops,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}", "traffic": None},
-        "pct_of_bf16_peak": 100.0 * achieved / peak,
+                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}", "traffic": None,
+                     "kernel": "dK/dV kernel alone (its 4 GEMMs: 2x the forward's FLOPs)",
+                     "kernel_ms_mean": dkdv_mean_ms},
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # prep + dK/dV + dQ kernels per step

@@ -23,7 +23,7 @@ FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
 EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_splitkv_plan", "fattn_bwd",
-            "fattn_status_string", "fattn_last_error", "fattn_version")
+            "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error", "fattn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +68,8 @@ def load_library():
             ]
             lib.fattn_fwd_host.restype = ctypes.c_int
             lib.fattn_fwd_host.argtypes = lib.fattn_fwd.argtypes
+            lib.fattn_set_kernel_events.restype = ctypes.c_int
+            lib.fattn_set_kernel_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
             lib.fattn_splitkv_plan.restype = ctypes.c_int
             lib.fattn_splitkv_plan.argtypes = [ctypes.c_int] * 6
             lib.fattn_bwd.restype = ctypes.c_int
@@ -104,6 +106,15 @@ def fwd_host_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
     """fattn_fwd_host with raw HOST addresses; returns the status code."""
     return load_library().fattn_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                                          float(scale), int(bool(causal)), key_len_ptr, stream)
+
+
+def set_kernel_events(start=None, stop=None) -> None:
+    """fattn_set_kernel_events with two torch.cuda.Event objects (created with
+    enable_timing=True and recorded once, so that their CUDA events exist), or
+    None, None to clear: the calling thread's next calls record them around
+    their dominant kernel."""
+    load_library().fattn_set_kernel_events(None if start is None else start.cuda_event,
+                                           None if stop is None else stop.cuda_event)
 
 
 def splitkv_plan(B: int, H: int, N: int, causal: bool, num_sms: int, n_splits: int = 0) -> int:

@@ -37,6 +37,17 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Events the calling thread asked to have recorded around the dominant
+// kernel of its calls (fattn_set_kernel_events); null: none.
+thread_local cudaEvent_t t_kernel_start = nullptr;
+thread_local cudaEvent_t t_kernel_stop = nullptr;
+void mark_kernel_start(cudaStream_t s) {
+  if (t_kernel_start) cudaEventRecord(t_kernel_start, s);
+}
+void mark_kernel_stop(cudaStream_t s) {
+  if (t_kernel_stop) cudaEventRecord(t_kernel_stop, s);
+}
 EncodeTiledFn g_encode = nullptr;
 unsigned long long g_wait_limit_ns = 0;
 
@@ -301,6 +312,7 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
   constexpr uint32_t smem = fattn::Cfg<D>::SMEM_BYTES;
   constexpr int nt = fattn::NUM_THREADS;
   const bool full = p.hd == D;
+  mark_kernel_start(stream);
   if (p.n_splits > 1 && full)
     fattn::fattn_fwd_kernel<D, true, true><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
   else if (p.n_splits > 1)
@@ -309,6 +321,7 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
     fattn::fattn_fwd_kernel<D, false, true><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
   else
     fattn::fattn_fwd_kernel<D, false, false><<<grid, nt, smem, stream>>>(mq, mk, mv, p);
+  mark_kernel_stop(stream);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   if (p.n_splits > 1) {
     constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 16);
@@ -350,10 +363,12 @@ int enqueue_d256(const void* q, const void* k, const void* v, fattn::Params p, v
   const double kv_head = 4.0 * (double)p.N * (double)p.hd;
   p.head_group = (int)std::max(1.0, std::min((double)BH, (48.0 * 1024 * 1024) / kv_head));
   constexpr uint32_t smem = fattn::D256Cfg::SMEM_BYTES;
+  mark_kernel_start(stream);
   if (full)
     fattn::fattn_fwd_d256_kernel<true><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
   else
     fattn::fattn_fwd_d256_kernel<false><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+  mark_kernel_stop(stream);
   return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
@@ -585,6 +600,12 @@ extern "C" FATTN_API int fattn_fwd_host(const void* q, const void* k, const void
   return rc;
 }
 
+extern "C" FATTN_API int fattn_set_kernel_events(void* start, void* stop) {
+  t_kernel_start = reinterpret_cast<cudaEvent_t>(start);
+  t_kernel_stop = reinterpret_cast<cudaEvent_t>(stop);
+  return FATTN_OK;
+}
+
 extern "C" FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits) {
   if (B <= 0 || H <= 0 || N <= 0 || num_sms <= 0 || n_splits < 0) return 0;
   return plan_splits(B, H, N, causal ? 1 : 0, num_sms, n_splits);
@@ -621,8 +642,10 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
       encode_map(&mdo, dout, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
     return FATTN_ERR_CUDA;
   const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
+  mark_kernel_start(stream);
   fattn::fattn_bwd_dkdv_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo,
                                                                                                       p);
+  mark_kernel_stop(stream);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   fattn::fattn_bwd_dq_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdDqCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv,
                                                                                                       mdo, p);

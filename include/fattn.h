@@ -198,6 +198,19 @@ FATTN_API int fattn_fwd_host(const void* q, const void* k, const void* v, void* 
  */
 FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits);
 
+/*
+ * fattn_set_kernel_events: measurement hook.  While set (non-NULL), every
+ * forward or backward call made by the calling thread records `start`
+ * (a cudaEvent_t) on its stream just before its dominant kernel and `stop`
+ * just after it: the attention kernel of the forward (not the V pre-pass or
+ * the split-KV combine; with fattn_fwd_host, around each chunk's, so the last
+ * chunk's pair remains) and the dK/dV kernel of the backward.  The events
+ * belong to the caller and must stay valid while set; cudaEventElapsedTime
+ * on them then gives that kernel's device time.  NULL, NULL clears the hook.
+ * Always returns FATTN_OK.
+ */
+FATTN_API int fattn_set_kernel_events(void* start, void* stop);
+
 /* A static, human-readable name for a status code. */
 FATTN_API const char* fattn_status_string(int status);
 

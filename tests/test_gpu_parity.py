@@ -169,3 +169,34 @@ def test_measured_workloads_sampled(cuda_device, name, n_full, n_rand):
     compare(o_g.reshape(-1, w.d)[rows], l_g.reshape(-1)[rows], o_r, l_r, name)
     # every output finite (no fully masked rows in these workloads)
     assert np.all(np.isfinite(o_g)) and np.all(np.isfinite(l_g))
+
+
+def test_kernel_event_hook(cuda_device):
+    """fattn_set_kernel_events: the library records the caller's events around
+    the attention kernel; its time is positive and inside the whole call's."""
+    import torch
+
+    from exact_softmax_attention_fattn_gb300 import binding
+    from tests.gpu_helpers import bits_to_device
+
+    x = make_inputs(Workload("hook", 2, 8, 2048, 128, True, 77))
+    q, k, v = (bits_to_device(a, cuda_device) for a in (x.q, x.k, x.v))
+    o = torch.empty_like(q)
+    lse = torch.empty((2, 8, 2048), dtype=torch.float32, device=cuda_device)
+    stream = torch.cuda.current_stream(cuda_device)
+    ks, ke, cs, ce = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    ks.record(stream)
+    ke.record(stream)
+    torch.cuda.synchronize(cuda_device)
+    binding.set_kernel_events(ks, ke)
+    cs.record(stream)
+    binding.forward_into(q, k, v, o, lse, causal=True)
+    ce.record(stream)
+    binding.set_kernel_events(None, None)
+    torch.cuda.synchronize(cuda_device)
+    t_kernel, t_call = ks.elapsed_time(ke), cs.elapsed_time(ce)
+    assert 0.0 < t_kernel <= t_call, (t_kernel, t_call)
+    # cleared: a later call leaves the events where they were
+    binding.forward_into(q, k, v, o, lse, causal=True)
+    torch.cuda.synchronize(cuda_device)
+    assert ks.elapsed_time(ke) == t_kernel
