@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(PREP_THREADS)
 // tiles each, and (dK/dV kernel) 512 bytes of LSE2 + 512 of D per stage.
 template <int D>
 struct BwdCfg {
-  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static_assert(D == 64 || D == 128, "head-dim bucket 64 or 128");
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t TILE_BYTES = 128u * D * 2u;
   static constexpr uint32_t FIX0_OFF = 0;                // K_j (dK/dV) or Q_i (dQ)

@@ -21,16 +21,19 @@
 //   * warp 8 (one lane) is the TMA producer: Q tiles into two fixed buffers,
 //     K and V tiles into a STAGES-deep ring, all 128-byte swizzled panels of
 //     64 columns;
-//   * warp 9 (one lane) issues tcgen05.mma: S_t = Q_t K_j^T (both operands in
-//     shared memory) and O_t += P_t V_j (P from tensor memory, V from shared
-//     memory), completion signalled with tcgen05.commit on mbarriers.  The two
+//   * warp 9 issues tcgen05.mma (the whole warp runs the loop, one elected
+//     lane issues): S_t = Q_t K_j^T (both operands in shared memory) and
+//     O_t += P_t V_j (P from tensor memory, V from shared memory), completion
+//     signalled with tcgen05.commit on mbarriers.  The two
 //     query tiles ping-pong: while one softmax group works on S_0, the tensor
 //     core runs the other tile's PV and S;
 //   * warps 0-3 and 4-7 are one softmax group per query tile, one thread per
 //     query row: the online-softmax step of the two-block derivation (running
 //     max m, normaliser l, rescaling of the unnormalised output by
 //     2^(m_old - m_new)), exponentials in base 2 with the scale folded in, P
-//     written back to tensor memory as bf16, then the final O / l and LSE.
+//     written back to tensor memory in the operand type of its V tile (fp16,
+//     or bf16 for a V tile outside fp16's range; see v_prepass.cuh), then the
+//     final O / l and LSE.
 //     The rescale of O is skipped while the running max has grown by less
 //     than 2^8 since the last rescale: O and l keep a common, slightly stale
 //     reference, so the final O / l is unchanged (exact up to rounding).
