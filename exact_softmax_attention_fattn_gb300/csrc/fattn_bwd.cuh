@@ -17,15 +17,19 @@
 //     and V_j stay in shared memory; Q_i, dO_i, LSE_i, D_i stream through a
 //     two-stage ring over the query tiles i that see tile j.  Per tile:
 //     S^T = K_j Q_i^T and dP^T = V_j dO_i^T in tensor memory (lanes = keys);
-//     four warps (one thread per key) form P^T = 2^(S^T c - LSE2) and
-//     dS^T = P^T (dP^T - D), store both as bf16 over the first 64 columns of
-//     their fp32 tiles, and the MMA issuer accumulates dV += P^T dO and
+//     eight warps in two groups (one thread per key in each; group g takes
+//     the 64 query columns [64g, 64g + 64)) form P^T = 2^(S^T c - LSE2) and
+//     dS^T = P^T (dP^T - D), each group storing its half as bf16 over the
+//     first 32 of its own 64 fp32 columns, and the MMA issuer accumulates dV += P^T dO and
 //     dK += dS^T Q in tensor memory (P^T, dS^T as the A operand from TMEM;
 //     dO, Q as MN-major B).  TMEM: S^T, dP^T, dV, dK = 4 x 128 columns.
 //   * fattn_bwd_dq_kernel: one CTA per (batch*head, 128-query tile i).  Q_i and
 //     dO_i stay; K_j, V_j stream over the key tiles i sees.  S = Q_i K_j^T,
-//     dP = dO_i V_j^T, then one thread per query row forms dS (bf16, over S)
-//     and dQ += dS K_j accumulates in tensor memory.
+//     dP = dO_i V_j^T, then two groups of four warps (one thread per query
+//     row in each, group g on the key columns [64g, 64g + 64)) form dS (bf16,
+//     over S) and dQ += dS K_j accumulates in tensor memory.  Every
+//     elementwise quantity has per-row or per-column constants only (LSE, D),
+//     so the column split needs no exchange between the groups.
 //   Splitting dQ from dK/dV costs two extra GEMMs per tile pair but needs no
 //   atomics: tensor memory cannot hold S, dP, dV, dK and a dQ accumulator at
 //   d = 128.  Every wait is bounded as in the forward kernel.
@@ -35,9 +39,12 @@
 
 namespace fattn {
 
-constexpr int BWD_THREADS = 192;   // warps 0-3 elementwise, 4 TMA producer, 5 MMA issuer
-constexpr int BWD_PRODUCER_WARP = 4;
-constexpr int BWD_MMA_WARP = 5;
+// warps 0-7 elementwise (two groups of four: group g takes the tile columns
+// [64g, 64g + 64) of the same TMEM lanes), 8 TMA producer, 9 MMA issuer
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_ELEM_WARPS = 8;
+constexpr int BWD_PRODUCER_WARP = 8;
+constexpr int BWD_MMA_WARP = 9;
 constexpr int BWD_STAGES = 2;
 constexpr int PREP_THREADS = 256;
 
@@ -144,11 +151,13 @@ struct BwdMma {
     });
   }
   // D(128 x D) (+)= A(128 x 128, bf16 in TMEM) B(128 x D, MN-major tile in shared memory).
+  // A is packed by the two elementwise groups into TMEM columns [0, 32) (its
+  // columns 0-63) and [64, 96) (its columns 64-127).
   __device__ __forceinline__ static void ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
     static_for<8>([&](auto kc) {
       constexpr int kk = decltype(kc)::value;
-      constexpr uint32_t boff = (kk * 2048u) >> 4;  // 16 rows = two 1024-byte row groups
-      constexpr uint32_t acol = 8u * kk;            // 16 columns of packed bf16 = 8 TMEM columns
+      constexpr uint32_t boff = (kk * 2048u) >> 4;            // 16 rows = two 1024-byte row groups
+      constexpr uint32_t acol = 8u * kk + (kk >= 4 ? 32u : 0u);  // 16 columns of packed bf16 = 8 TMEM columns
       mma_ts_w_off<boff, acol>(d_tmem, a_tmem, b_desc, IDESC_ACC, kk > 0 ? 1u : accumulate);
     });
   }
@@ -160,37 +169,39 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-// Rows [key0, key0 + 128) of an accumulator in TMEM -> bf16 rows of `out`
-// ([B*H, N, hd]: the first hd of the D accumulator columns), times `mul`;
-// rows at or past N are skipped.
+// The elementwise group g's share of an accumulator's row: the 64-column
+// blocks hcol = g, g + 2, ... (all of them at D = 128: one each; at D = 64
+// group 0 stores the only block).
 template <int D>
-__device__ __forceinline__ void store_acc_rows(uint32_t t_addr, float mul, __nv_bfloat16* out, size_t row_flat,
-                                               bool row_ok, int hd) {
+__device__ __forceinline__ void store_acc_part(uint32_t t_addr, float mul, __nv_bfloat16* out, size_t row_flat,
+                                               bool row_ok, int hd, int g) {
   uint4* dst = reinterpret_cast<uint4*>(out + row_flat * hd);
 #pragma unroll
   for (int hcol = 0; hcol < D / 64; ++hcol) {
+    if (hcol % 2 != g) continue;
     uint32_t av[64];
     tmem_ld64(t_addr + 64u * hcol, av);
     tmem_ld_wait(av);
-    uint32_t ob[32];
-#pragma unroll
-    for (int x = 0; x < 32; ++x) ob[x] = pack_bf16x2(__uint_as_float(av[2 * x]) * mul, __uint_as_float(av[2 * x + 1]) * mul);
     if (row_ok) {
 #pragma unroll
       for (int x = 0; x < 8; ++x)
         if (64 * hcol + 8 * x < hd)
-          dst[8 * hcol + x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
+          dst[8 * hcol + x] = make_uint4(
+              pack_bf16x2(__uint_as_float(av[8 * x]) * mul, __uint_as_float(av[8 * x + 1]) * mul),
+              pack_bf16x2(__uint_as_float(av[8 * x + 2]) * mul, __uint_as_float(av[8 * x + 3]) * mul),
+              pack_bf16x2(__uint_as_float(av[8 * x + 4]) * mul, __uint_as_float(av[8 * x + 5]) * mul),
+              pack_bf16x2(__uint_as_float(av[8 * x + 6]) * mul, __uint_as_float(av[8 * x + 7]) * mul));
     }
   }
 }
 
 template <int D>
-__device__ __forceinline__ void store_zero_rows(__nv_bfloat16* out, size_t row_flat, bool row_ok, int hd) {
+__device__ __forceinline__ void store_zero_part(__nv_bfloat16* out, size_t row_flat, bool row_ok, int hd, int g) {
   if (!row_ok) return;
   uint4* dst = reinterpret_cast<uint4*>(out + row_flat * hd);
 #pragma unroll
   for (int x = 0; x < D / 8; ++x)
-    if (8 * x < hd) dst[x] = make_uint4(0, 0, 0, 0);
+    if ((x / 8) % 2 == g && 8 * x < hd) dst[x] = make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ int clamp_kl(const BwdParams& p, int b) {
@@ -234,8 +245,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
-    mbar_init(bar(C::B_OPS_READY), 128);
-    mbar_init(bar(C::B_DS_READY), 128);
+    mbar_init(bar(C::B_OPS_READY), 32 * BWD_ELEM_WARPS);
+    mbar_init(bar(C::B_DS_READY), 32 * BWD_ELEM_WARPS);
     mbar_init(bar(C::B_ACC_FULL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -353,20 +364,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mma_commit_w(bar(C::B_DRAIN));
       drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
     }
-  } else if (warp < 4) {
+  } else if (warp < BWD_ELEM_WARPS) {
     waiter.role = ROLE_SOFTMAX;
-    const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
+    const int g = warp / 4;             // column group: tile columns [64g, 64g + 64)
+    const int quarter = warp % 4;       // TMEM lane quarter
+    const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane
     const int key = key0 + r;
     const bool key_vis = key < kl;
     const size_t row_flat = (size_t)bh * (size_t)p.N + (size_t)key;
     const bool row_ok = key < p.N;
     if (n_q == 0) {
-      store_zero_rows<D>(p.dv, row_flat, row_ok, p.hd);
-      store_zero_rows<D>(p.dk, row_flat, row_ok, p.hd);
+      store_zero_part<D>(p.dv, row_flat, row_ok, p.hd, g);
+      store_zero_part<D>(p.dk, row_flat, row_ok, p.hd, g);
     } else {
-      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-      const uint32_t s_addr = tmem + lane_off + BT_S;
-      const uint32_t dp_addr = tmem + lane_off + BT_DP;
+      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      // this group's 64 columns of S^T and dP^T; P^T and dS^T are packed over
+      // the first 32 of them (the other group's columns are never touched)
+      const uint32_t s_addr = tmem + lane_off + BT_S + 64u * (uint32_t)g;
+      const uint32_t dp_addr = tmem + lane_off + BT_DP + 64u * (uint32_t)g;
       const float c = p.scale_log2;
       bool ok = true;
       for (int n = 0; ok && n < n_q; ++n) {
@@ -377,36 +392,35 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float4* lse4 = reinterpret_cast<const float4*>(base_ptr + C::ROWS_OFF + (uint32_t)s * 1024u);
+        const float4* lse4 = reinterpret_cast<const float4*>(base_ptr + C::ROWS_OFF + (uint32_t)s * 1024u) + 16 * g;
         const float4* del4 = lse4 + 32;
         // visible columns: query q0 + col sees this key iff the key is inside
         // key_len and (causal) key <= query; rows past N read as zero and
         // contribute nothing (their dO and Q are zero)
         const int min_q = p.causal ? key - q0 : 0;  // columns < min_q are masked
-        const bool any_mask = !key_vis || min_q > 0;
+        const bool any_mask = !key_vis || min_q > 64 * g;
         // phase 1: P^T (kept in fp32 for dS^T), released for dV as soon as it is stored
-        float pr[128];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        float pr[64];
+        {
           uint32_t sh[64];
-          tmem_ld64(s_addr + 64u * h, sh);
+          tmem_ld64(s_addr, sh);
           tmem_ld_wait(sh);
           uint32_t pk[32];
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 l4 = lse4[16 * h + q4];
+            const float4 l4 = lse4[q4];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int col = 64 * h + 4 * q4 + e;
+              const int col = 64 * g + 4 * q4 + e;
               float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
               if (any_mask) pe = (key_vis && col >= min_q) ? pe : 0.0f;
-              pr[col] = pe;
+              pr[4 * q4 + e] = pe;
             }
-            pk[2 * q4] = pack_bf16x2(pr[64 * h + 4 * q4], pr[64 * h + 4 * q4 + 1]);
-            pk[2 * q4 + 1] = pack_bf16x2(pr[64 * h + 4 * q4 + 2], pr[64 * h + 4 * q4 + 3]);
+            pk[2 * q4] = pack_bf16x2(pr[4 * q4], pr[4 * q4 + 1]);
+            pk[2 * q4 + 1] = pack_bf16x2(pr[4 * q4 + 2], pr[4 * q4 + 3]);
           }
-          tmem_st32(s_addr + 32u * h, pk);
+          tmem_st32(s_addr, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -416,23 +430,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        {
           uint32_t dh[64];
-          tmem_ld64(dp_addr + 64u * h, dh);
+          tmem_ld64(dp_addr, dh);
           tmem_ld_wait(dh);
           uint32_t dk2[32];
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 d4 = del4[16 * h + q4];
+            const float4 d4 = del4[q4];
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
             float dsv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dsv[e] = pr[64 * h + 4 * q4 + e] * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
+            for (int e = 0; e < 4; ++e) dsv[e] = pr[4 * q4 + e] * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
             dk2[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
             dk2[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
           }
-          tmem_st32(dp_addr + 32u * h, dk2);
+          tmem_st32(dp_addr, dk2);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -444,12 +457,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        store_acc_rows<D>(tmem + lane_off + BT_ACC0, 1.0f, p.dv, row_flat, row_ok, p.hd);
-        store_acc_rows<D>(tmem + lane_off + BT_ACC0 + D, p.scale, p.dk, row_flat, row_ok, p.hd);
+        store_acc_part<D>(tmem + lane_off + BT_ACC0, 1.0f, p.dv, row_flat, row_ok, p.hd, g);
+        store_acc_part<D>(tmem + lane_off + BT_ACC0 + D, p.scale, p.dk, row_flat, row_ok, p.hd, g);
       }
     }
   }
-
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_S_FULL + 1), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
-    mbar_init(bar(C::B_DS_READY), 128);
+    mbar_init(bar(C::B_DS_READY), 32 * BWD_ELEM_WARPS);
     mbar_init(bar(C::B_ACC_FULL), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -658,17 +670,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mma_commit_w(bar(C::B_DRAIN));
       drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
     }
-  } else if (warp < 4) {
+  } else if (warp < BWD_ELEM_WARPS) {
     waiter.role = ROLE_SOFTMAX;
-    const int r = warp * 32 + lane;  // query row within the tile = TMEM lane
+    const int g = warp / 4;             // column group: tile columns (keys) [64g, 64g + 64)
+    const int quarter = warp % 4;       // TMEM lane quarter
+    const int r = quarter * 32 + lane;  // query row within the tile = TMEM lane
     const int query = q0 + r;
     const size_t row_flat = (size_t)bh * (size_t)p.N + (size_t)query;
     const bool row_ok = query < p.N;
     if (n_k == 0) {
-      store_zero_rows<D>(p.dq, row_flat, row_ok, p.hd);
+      store_zero_part<D>(p.dq, row_flat, row_ok, p.hd, g);
     } else {
-      const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-      const uint32_t dp_addr = tmem + lane_off + BQ_DP;
+      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      const uint32_t dp_addr = tmem + lane_off + BQ_DP + 64u * (uint32_t)g;
       const float c = p.scale_log2;
       const size_t prow = (size_t)bh * (size_t)p.N_pad + (size_t)query;
       const float lse2 = p.lse2[prow];
@@ -677,43 +691,42 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int lim = p.causal ? min(kl, query + 1) : kl;
       bool ok = true;
       for (int n = 0; ok && n < n_k; ++n) {
-        const uint32_t s_addr = tmem + lane_off + BQ_S0 + 128u * (uint32_t)(n & 1);
+        // this group's 64 columns of S_n; dS is packed over the first 32 of them
+        const uint32_t s_addr = tmem + lane_off + BQ_S0 + 128u * (uint32_t)(n & 1) + 64u * (uint32_t)g;
         ok = wait_bar(waiter, bar(C::B_S_FULL + (n & 1)), (n >> 1) & 1, C::B_S_FULL + (n & 1), u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const int vis_n = lim - n * 128;  // columns [0, vis_n) visible
-        const bool masked = vis_n < 128;
+        const int vis_n = lim - n * 128 - 64 * g;  // this group's columns [0, vis_n) visible
+        const bool masked = vis_n < 64;
         // phase 1 (while dP is computed): P in fp32 registers
-        float pr[128];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        float pr[64];
+        {
           uint32_t sh[64];
-          tmem_ld64(s_addr + 64u * h, sh);
+          tmem_ld64(s_addr, sh);
           tmem_ld_wait(sh);
 #pragma unroll
           for (int q = 0; q < 64; ++q) {
             float pe = ex2(fmaf(__uint_as_float(sh[q]), c, -lse2));
-            if (masked) pe = 64 * h + q < vis_n ? pe : 0.0f;
-            pr[64 * h + q] = pe;
+            if (masked) pe = q < vis_n ? pe : 0.0f;
+            pr[q] = pe;
           }
         }
-        // phase 2: dS = P (dP - D), stored as bf16 over the first 64 columns of S
+        // phase 2: dS = P (dP - D), stored as bf16 over this group's first 32 columns of S
         ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        {
           uint32_t dh[64];
-          tmem_ld64(dp_addr + 64u * h, dh);
+          tmem_ld64(dp_addr, dh);
           tmem_ld_wait(dh);
           uint32_t pk[32];
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            pk[q] = pack_bf16x2(pr[64 * h + 2 * q] * (__uint_as_float(dh[2 * q]) - drow),
-                                pr[64 * h + 2 * q + 1] * (__uint_as_float(dh[2 * q + 1]) - drow));
-          tmem_st32(s_addr + 32u * h, pk);
+            pk[q] = pack_bf16x2(pr[2 * q] * (__uint_as_float(dh[2 * q]) - drow),
+                                pr[2 * q + 1] * (__uint_as_float(dh[2 * q + 1]) - drow));
+          tmem_st32(s_addr, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -725,11 +738,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        store_acc_rows<D>(tmem + lane_off + BQ_DQ, p.scale, p.dq, row_flat, row_ok, p.hd);
+        store_acc_part<D>(tmem + lane_off + BQ_DQ, p.scale, p.dq, row_flat, row_ok, p.hd, g);
       }
     }
   }
-
   __syncwarp();
   tc_fence_before();
   __syncthreads();
