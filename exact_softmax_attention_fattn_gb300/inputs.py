@@ -166,6 +166,59 @@ WORKLOADS: dict[str, Workload] = {
 HEADLINE = "b2h16n4096d128_causal"
 
 
+@dataclasses.dataclass(frozen=True)
+class LinearWorkload:
+    """A causal linear attention problem: Q, K [B, H, N, E] and V [B, H, N, M],
+    float32 N(0, 1), optional per-batch key lengths uniform in key_len_range."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    E: int
+    M: int
+    seed: int
+    key_len_range: tuple[int, int] | None = None
+
+
+@dataclasses.dataclass
+class LinearInputs:
+    w: LinearWorkload
+    q: np.ndarray  # float32 [B, H, N, E]
+    k: np.ndarray  # float32 [B, H, N, E]
+    v: np.ndarray  # float32 [B, H, N, M]
+    key_len: np.ndarray | None
+
+
+def make_linear_inputs(w: LinearWorkload) -> LinearInputs:
+    qk = w.B * w.H * w.N * w.E
+    q = normal(w.seed, STREAM_Q, qk).reshape(w.B, w.H, w.N, w.E)
+    k = normal(w.seed, STREAM_K, qk).reshape(w.B, w.H, w.N, w.E)
+    v = normal(w.seed, STREAM_V, w.B * w.H * w.N * w.M).reshape(w.B, w.H, w.N, w.M)
+    key_len = None
+    if w.key_len_range is not None:
+        lo, hi = w.key_len_range
+        z = splitmix64(w.seed, STREAM_KEYLEN, 0, w.B)
+        key_len = (lo + (z % np.uint64(hi - lo + 1)).astype(np.int64)).astype(np.int32)
+    return LinearInputs(w, q, k, v, key_len)
+
+
+# Causal linear attention (the second workload): a language-model head shape
+# at the feature size the page's kernels dispatch on (E = M = 64).
+LINEAR_WORKLOADS: dict[str, LinearWorkload] = {
+    "lin_b2h16n4096e64": LinearWorkload("lin_b2h16n4096e64", 2, 16, 4096, 64, 64, 8),
+    "lin_b8h8n2048e64_keylen": LinearWorkload("lin_b8h8n2048e64_keylen", 8, 8, 2048, 64, 64, 9,
+                                              key_len_range=(1024, 2048)),
+}
+
+
+def linear_flops(w: LinearWorkload) -> float:
+    """Algorithmic FLOPs of the causal linear attention forward, the page's
+    recurrence: per row, the state update k v^T and the read q^T S (2 E M
+    multiply-adds), and the normaliser's q . s and cumulative key sum (2 E)."""
+    return float(w.B * w.H * w.N) * (4.0 * w.E * w.M + 4.0 * w.E)
+
+
 def causal_flops(w: Workload, key_len: np.ndarray | None = None) -> float:
     """Algorithmic FLOPs of one forward: 4*B*H*N^2*d, half of it when causal;
     with key padding, 4*H*N*d*sum(key_len)."""

@@ -3,4 +3,4 @@
 TEST INFRASTRUCTURE ONLY: imported by tests/, the smoke check and the
 benchmark's CPU-baseline and reference legs, never by the product path.
 """
-from .oracle import Oracle, backward, build, compile_source, default_threads, forward, probs  # noqa: F401
+from .oracle import Oracle, backward, build, compile_source, default_threads, forward, linear, probs  # noqa: F401

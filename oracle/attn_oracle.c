@@ -450,3 +450,94 @@ int fattn_oracle_backward(const uint16_t *q, const uint16_t *k, const uint16_t *
     free(priv);
     return rc;
 }
+
+/*
+ * Causal linear attention, plain fp64 CPU oracle (the second workload).
+ *
+ * What it computes ("Linear Attention CUDA kernel" page: the kernel feature
+ * map phi(x) = elu(x) + 1 of the linear transformer, the key-length mask of
+ * CausalLinearAttention.forward, which multiplies the mapped keys by the
+ * per-position 0/1 length matrix, and the causal dot product of its CPU
+ * implementation, which walks the sequence keeping a running outer-product
+ * state), for every (b, h):
+ *     kt_j = phi(k_j) if j < key_len[b] else 0,   qt_i = phi(q_i)
+ *     state S_i = sum_{j <= i} kt_j v_j^T   (E x M),   s_i = sum_{j <= i} kt_j
+ *     out_i = (qt_i^T S_i) / (qt_i . s_i + eps)
+ * -- the page's numerator V'_i = sum_{j <= i} (qt_i . kt_j) v_j times its
+ * normaliser Z_i = 1 / (qt_i . cumsum(kt)_i + eps).
+ * Inputs are float32 (the page's kernels take float tensors), widened to double.
+ */
+typedef struct {
+    const float *q, *k, *v;
+    int64_t H, N, E, M;
+    const int32_t *key_len;
+    double eps;
+    double *out;
+    int64_t head_begin, head_end;
+    int status;
+} lin_job;
+
+static double phi_elu1(double x) { return x > 0.0 ? x + 1.0 : exp(x); } /* elu(x) + 1 */
+
+static void *lin_worker(void *arg) {
+    lin_job *J = (lin_job *)arg;
+    const int64_t E = J->E, M = J->M, N = J->N;
+    double *S = (double *)malloc((size_t)(E * M + 2 * E) * sizeof(double));
+    if (!S) {
+        J->status = 2;
+        return NULL;
+    }
+    double *s = S + E * M, *kt = s + E;
+    for (int64_t hs = J->head_begin; hs < J->head_end; ++hs) {
+        const int64_t b = hs / J->H;
+        int64_t kl = J->key_len ? J->key_len[b] : N;
+        if (kl < 0) kl = 0;
+        if (kl > N) kl = N;
+        for (int64_t x = 0; x < E * M + E; ++x) S[x] = 0.0;
+        const float *qh = J->q + hs * N * E, *kh = J->k + hs * N * E, *vh = J->v + hs * N * M;
+        double *oh = J->out + hs * N * M;
+        for (int64_t i = 0; i < N; ++i) {
+            /* the state takes row i's key and value (a masked key adds nothing) */
+            for (int64_t e = 0; e < E; ++e) kt[e] = i < kl ? phi_elu1((double)kh[i * E + e]) : 0.0;
+            for (int64_t e = 0; e < E; ++e) {
+                s[e] += kt[e];
+                for (int64_t m = 0; m < M; ++m) S[e * M + m] += kt[e] * (double)vh[i * M + m];
+            }
+            /* row i's output from the state */
+            double den = J->eps;
+            for (int64_t m = 0; m < M; ++m) oh[i * M + m] = 0.0;
+            for (int64_t e = 0; e < E; ++e) {
+                const double qt = phi_elu1((double)qh[i * E + e]);
+                den += qt * s[e];
+                for (int64_t m = 0; m < M; ++m) oh[i * M + m] += qt * S[e * M + m];
+            }
+            for (int64_t m = 0; m < M; ++m) oh[i * M + m] /= den;
+        }
+    }
+    free(S);
+    return NULL;
+}
+
+int fattn_oracle_linear(const float *q, const float *k, const float *v, int64_t B, int64_t H, int64_t N, int64_t E,
+                        int64_t M, const int32_t *key_len, double eps, double *out, int threads) {
+    if (B < 0 || H < 0 || N < 0 || E <= 0 || M <= 0) return 1;
+    const int64_t heads = B * H;
+    if (heads == 0 || N == 0) return 0;
+    int nw = threads < 1 ? 1 : threads;
+    if (nw > 256) nw = 256;
+    if (nw > heads) nw = (int)heads;
+    lin_job jobs[256];
+    pthread_t tids[256];
+    int started[256];
+    int rc = 0;
+    for (int w = 0; w < nw; ++w) {
+        jobs[w] = (lin_job){q, k, v, H, N, E, M, key_len, eps, out, heads * w / nw, heads * (w + 1) / nw, 0};
+        started[w] = (nw > 1) && pthread_create(&tids[w], NULL, lin_worker, &jobs[w]) == 0;
+        if (!started[w]) lin_worker(&jobs[w]);
+    }
+    for (int w = 0; w < nw; ++w) {
+        if (started[w]) pthread_join(tids[w], NULL);
+        if (jobs[w].status) rc = jobs[w].status;
+    }
+    return rc;
+}

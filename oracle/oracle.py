@@ -1,4 +1,5 @@
-"""Plain fp64 CPU oracle for the exact softmax attention forward and backward.
+"""Plain fp64 CPU oracle for the exact softmax attention forward and backward,
+and for causal linear attention (the second workload).
 
 TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 benchmark's CPU-baseline / reference leg import this module.  The product path
@@ -54,6 +55,12 @@ def _bind(path: str):
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
+    lib.fattn_oracle_linear.restype = ctypes.c_int
+    lib.fattn_oracle_linear.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
     ]
     lib.fattn_oracle_probs.restype = ctypes.c_int
     lib.fattn_oracle_probs.argtypes = [
@@ -189,6 +196,37 @@ def probs(q, k, scale: float, causal: bool, key_len=None, b: int = 0, h: int = 0
     return p, s
 
 
+def linear(q, k, v, key_len=None, eps: float = 1e-6, threads: int | None = None, _lib_override=None):
+    """Causal linear attention in fp64 (the "Linear Attention CUDA kernel"
+    page: phi = elu + 1 on queries and keys, keys past key_len[b] zeroed, the
+    running outer-product state of its CPU causal dot product, and the
+    normaliser 1 / (phi(q_i) . cumsum(phi(k))_i + eps) of
+    CausalLinearAttention.forward).
+
+    q, k: float32 [B, H, N, E]; v: float32 [B, H, N, M]; key_len: int32 [B]
+    or None.  Returns float64 [B, H, N, M].
+    """
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    if q.ndim != 4 or k.shape != q.shape or v.ndim != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B, H, N, E] and v [B, H, N, M]")
+    B, H, N, E = q.shape
+    M = v.shape[3]
+    kl = None
+    if key_len is not None:
+        kl = np.ascontiguousarray(key_len, dtype=np.int32)
+        if kl.shape != (B,):
+            raise ValueError("key_len must have shape [B]")
+    out = np.empty((B, H, N, M), dtype=np.float64)
+    rc = (_lib_override or _load()).fattn_oracle_linear(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, N, E, M, kl.ctypes.data if kl is not None else None,
+        float(eps), out.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle linear failed with code {rc}")
+    return out
+
+
 class Oracle:
     """forward()/probs() bound to one compiled copy of attn_oracle.c (the test
     suite uses this to run its pins against deliberately broken copies)."""
@@ -198,6 +236,9 @@ class Oracle:
 
     def forward(self, *a, **kw):
         return forward(*a, _lib_override=self._lib, **kw)
+
+    def linear(self, *a, **kw):
+        return linear(*a, _lib_override=self._lib, **kw)
 
     def probs(self, *a, **kw):
         return probs(*a, _lib_override=self._lib, **kw)
