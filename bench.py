@@ -56,7 +56,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from exact_softmax_attention_fattn_gb300.inputs import HEADLINE, WORKLOADS, causal_flops, make_inputs  # noqa: E402
+from exact_softmax_attention_fattn_gb300.inputs import (  # noqa: E402
+    HEADLINE, LINEAR_WORKLOADS, WORKLOADS, causal_flops, make_inputs)
 
 KERNEL_NAME = "fattn_fwd_kernel"
 METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 bf16 dense peak"
@@ -403,6 +404,127 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     print(json.dumps(line), flush=True)
 
 
+def linear_arm(args, rank: int, world: int, local_rank: int):
+    """--pass linear: causal linear attention (fattn_linear_fwd, fp32) on one
+    of LINEAR_WORKLOADS, timed like the forward; FLOPs are the page's
+    recurrence (linear_flops); the roofline is the output kernel's, against the
+    fp32 CUDA-core peak (152 SMs x 128 lanes x 2 FLOP x the sampled max SM
+    clock), since these kernels run on the CUDA cores."""
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    from exact_softmax_attention_fattn_gb300 import binding
+    from exact_softmax_attention_fattn_gb300.inputs import LINEAR_WORKLOADS, linear_flops, make_linear_inputs
+
+    name = args.workload if args.workload in LINEAR_WORKLOADS else "lin_b2h16n4096e64"
+    w = LINEAR_WORKLOADS[name]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    x = make_linear_inputs(w)
+    q, k, v = (torch.from_numpy(a).to(dev) for a in (x.q, x.k, x.v))
+    kl = None if x.key_len is None else torch.from_numpy(x.key_len).to(dev)
+    out = torch.empty((w.B, w.H, w.N, w.M), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = linear_flops(w)
+
+    def step():
+        binding.linear_forward(q, k, v, key_len=kl, out=out)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    untimed = warm_up(step, flush, args.warmup, sampler, dev)
+    st, detail = binding.last_error(stream)
+    if st != binding.FATTN_OK:
+        raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kev = kernel_event_pairs(args.steps, stream)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        binding.set_kernel_events(*kev[i])
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    binding.set_kernel_events(None, None)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    st, detail = binding.last_error(stream)
+    if st != binding.FATTN_OK:
+        raise RuntimeError(f"kernel reported {binding.status_string(st)} {detail}")
+    step_ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    out_ms = [a.elapsed_time(b) for a, b in kev]
+    ms_per_step, value = aggregate_ranks(float(sum(step_ms)), flops, args.steps, world, dev)
+
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        qd, kd, vd = (torch.empty_like(t) for t in (q, k, v))
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            binding.linear_forward(qd, kd, vd, key_len=kl, out=out)
+            oh.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(2):
+            e2e_step()
+        n_e2e = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        e2e = {"value": flops / e2e_s / 1e12 * world, "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * 4 for t in (q, k, v)), "d2h_bytes_per_step": out.numel() * 4,
+               "ms_per_step": e2e_s * 1e3}
+    if rank != 0:
+        return
+    sm_max = (clocks or {}).get("sm_max_mhz") or 2070.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * 128 * 2 * sm_max * 1e6 / 1e12  # fp32 FMA lanes x 2 FLOP x clock
+    out_mean = float(np.mean(out_ms))
+    achieved = flops / (out_mean * 1e-3) / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        oracle.linear(x.q[:1, :1], x.k[:1, :1], x.v[:1, :1], key_len=None if x.key_len is None else x.key_len[:1])
+        dt = time.perf_counter() - t0
+        cpu = {"value": flops / (w.B * w.H) / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
+               "kind": "oracle", "sample": f"head 0 of {w.B * w.H} ({name}), full fp64 recurrence",
+               "seconds": round(dt, 3)}
+    line = {
+        "metric": "causal linear attention TFLOP/s (the recurrence's 4*E*M + 4*E FLOPs per row)",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "untimed_steps": untimed, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded SplitMix64/Box-Muller, float32)",
+        "config": {"workload": name, "pass": "linear", "B": w.B, "H": w.H, "N": w.N, "E": w.E, "M": w.M,
+                   "key_padding": x.key_len is not None, "flops_per_step": flops,
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "peak_kind": "fp32 CUDA-core FMA peak derived from SMs x 128 lanes x 2 x max SM clock",
+                     "traffic": None, "kernel": "fattn_linear_output_kernel alone", "kernel_ms_mean": out_mean},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,  # chunk state, scan, output
+        "kernel": "fattn_linear_state_kernel + fattn_linear_scan_kernel + fattn_linear_output_kernel",
+        "kernel_ms": {"min": min(step_ms), "median": float(np.median(step_ms)), "max": max(step_ms)},
+        "wall_s_timed_region": wall,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def bwd_arm(args, rank: int, world: int, local_rank: int):
     """The backward pass, timed like the forward (one JSON line on rank 0)."""
     import torch
@@ -528,12 +650,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(LINEAR_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="time the forward (default) or the backward")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "linear"], default="fwd",
+                    help="time the forward (default), the backward, or causal linear attention")
     ap.add_argument("--splits", type=int, default=None,
                     help="forward: force this many key splits per query block (split-KV; 1 = none); "
                          "default: the library's choice")
@@ -554,7 +676,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        (bwd_arm if args.pass_ == "bwd" else our_arm)(args, rank, world, local_rank)
+        {"bwd": bwd_arm, "linear": linear_arm}.get(args.pass_, our_arm)(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -23,7 +23,8 @@ FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
 EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_splitkv_plan", "fattn_bwd",
-            "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error", "fattn_version")
+            "fattn_linear_fwd", "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error",
+            "fattn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +69,9 @@ def load_library():
             ]
             lib.fattn_fwd_host.restype = ctypes.c_int
             lib.fattn_fwd_host.argtypes = lib.fattn_fwd.argtypes
+            lib.fattn_linear_fwd.restype = ctypes.c_int
+            lib.fattn_linear_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [
+                ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]
             lib.fattn_set_kernel_events.restype = ctypes.c_int
             lib.fattn_set_kernel_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
             lib.fattn_splitkv_plan.restype = ctypes.c_int
@@ -106,6 +110,44 @@ def fwd_host_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
     """fattn_fwd_host with raw HOST addresses; returns the status code."""
     return load_library().fattn_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                                          float(scale), int(bool(causal)), key_len_ptr, stream)
+
+
+def linear_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, B: int, H: int, N: int, E: int, M: int,
+               key_len_ptr: int | None, eps: float, stream: int | None) -> int:
+    """fattn_linear_fwd with raw addresses; returns the status code."""
+    return load_library().fattn_linear_fwd(q_ptr, k_ptr, v_ptr, out_ptr, int(B), int(H), int(N), int(E), int(M),
+                                           key_len_ptr, float(eps), stream)
+
+
+def linear_forward(q, k, v, key_len=None, eps: float = 1e-6, out=None, stream=None):
+    """Causal linear attention (fattn_linear_fwd) on fp32 device tensors
+    q, k [B, H, N, E] and v [B, H, N, M]: returns (or fills) out [B, H, N, M],
+    enqueued on `stream` (default: the current stream)."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.float32 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor of rank 4")
+    B, H, N, E = q.shape
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("k must be shaped like q, v like q up to its last dimension")
+    M = v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=torch.float32, device=q.device)
+    elif out.shape != (B, H, N, M) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor [B, H, N, M]")
+    kl_ptr = None
+    if key_len is not None:
+        kl = torch.as_tensor(key_len, dtype=torch.int32).to(q.device).contiguous()
+        if kl.shape != (B,):
+            raise ValueError("key_len must hold B values")
+        kl_ptr = kl.data_ptr()
+    with torch.cuda.device(q.device):
+        handle = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+        st = linear_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N, E, M, kl_ptr, eps, handle)
+    if st != FATTN_OK:
+        raise FattnError(st, "fattn_linear_fwd")
+    return out
 
 
 def set_kernel_events(start=None, stop=None) -> None:

@@ -15,6 +15,7 @@
 #include "fattn_bwd.cuh"
 #include "fattn_d256.cuh"
 #include "fattn_kernel.cuh"
+#include "linear_attn.cuh"
 #include "splitkv_combine.cuh"
 #include "v_prepass.cuh"
 
@@ -91,6 +92,18 @@ int configure_d256_kernel() {
              : FATTN_ERR_CUDA;
 }
 
+// The linear-attention kernels' shared memory, at the largest feature sizes.
+int configure_linear_kernels() {
+  const fattn::LinSmem L(128, 128);
+  const int state_bytes = ((fattn::LIN_C * 129 + 3) / 4 * 4 + fattn::LIN_C * 128) * 4;
+  return cudaFuncSetAttribute(fattn::fattn_linear_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              state_bytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_linear_output_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, L.total * 4) == cudaSuccess
+             ? FATTN_OK
+             : FATTN_ERR_CUDA;
+}
+
 template <int D>
 int configure_kernel() {
   int rc = configure_fwd_kernel<D, false, true>();
@@ -141,6 +154,7 @@ int device_state(int dev, DeviceState** out) {
     if (rc == FATTN_OK) rc = configure_kernel<128>();
     if (rc == FATTN_OK) rc = configure_d256_kernel<true>();
     if (rc == FATTN_OK) rc = configure_d256_kernel<false>();
+    if (rc == FATTN_OK) rc = configure_linear_kernels();
     if (rc != FATTN_OK) return rc;
     if (make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
     if (cudaMalloc(&s.err, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
@@ -597,6 +611,68 @@ extern "C" FATTN_API int fattn_fwd_host(const void* q, const void* k, const void
   if (cudaFreeAsync(buf, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   for (auto& e : ev)
     if (e) cudaEventDestroy(e);
+  return rc;
+}
+
+// ------------------------------------------------------------------------
+// fattn_linear_fwd: causal linear attention (the second workload).
+extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const float* v, float* out, int B, int H,
+                                          int N, int E, int M, const int32_t* key_len, float eps, void* stream) {
+  if (B < 0 || H < 0 || N < 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.0f) return FATTN_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FATTN_OK;
+  if (!q || !k || !v || !out) return FATTN_ERR_INVALID_ARG;
+  if (E < 4 || E > 128 || E % 4 || M < 4 || M > 128 || M % 4) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - fattn::LIN_C) return FATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4) || (key_len && !aligned(key_len, 4)))
+    return FATTN_ERR_INVALID_ARG;
+  if (!is_device_pointer(q) || !is_device_pointer(k) || !is_device_pointer(v) || !is_device_pointer(out) ||
+      (key_len && !is_device_pointer(key_len)))
+    return FATTN_ERR_INVALID_ARG;
+  const long long BH = (long long)B * H;
+  const int n_chunks = (N + fattn::LIN_C - 1) / fattn::LIN_C;
+  const int blocks_per_head = (E * M + E + fattn::LIN_THREADS - 1) / fattn::LIN_THREADS;
+  if (BH * n_chunks > 0x7FFFFFFFll || BH * blocks_per_head > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  DeviceState* ds = nullptr;
+  int rc = device_state(dev, &ds);
+  if (rc != FATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t state_floats = (size_t)BH * n_chunks * (size_t)E * M;
+  const size_t ksum_floats = (size_t)BH * n_chunks * (size_t)E;
+  void* scratch = nullptr;
+  if (cudaMallocFromPoolAsync(&scratch, round_up(state_floats * 4u, 256) + round_up(ksum_floats * 4u, 256), ds->pool,
+                              s) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  fattn::LinParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.key_len = key_len;
+  p.state = reinterpret_cast<float*>(scratch);
+  p.ksum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scratch) + round_up(state_floats * 4u, 256));
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.E = E;
+  p.M = M;
+  p.n_chunks = n_chunks;
+  p.eps = eps;
+  const int state_smem = ((fattn::LIN_C * (E + 1) + 3) / 4 * 4 + fattn::LIN_C * M) * 4;
+  const int out_smem = fattn::LinSmem(E, M).total * 4;
+  fattn::fattn_linear_state_kernel<<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, state_smem, s>>>(p);
+  fattn::fattn_linear_scan_kernel<<<(unsigned)(BH * blocks_per_head), fattn::LIN_THREADS, 0, s>>>(p,
+                                                                                                   blocks_per_head);
+  mark_kernel_start(s);
+  fattn::fattn_linear_output_kernel<<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, out_smem, s>>>(p);
+  mark_kernel_stop(s);
+  if (cudaGetLastError() != cudaSuccess) rc = FATTN_ERR_CUDA;
+  if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }
 

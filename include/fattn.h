@@ -199,12 +199,44 @@ FATTN_API int fattn_fwd_host(const void* q, const void* k, const void* v, void* 
 FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits);
 
 /*
+ * fattn_linear_fwd: causal linear attention, the second workload ("Linear
+ * Attention CUDA kernel" page: CausalLinearAttention.forward with its causal
+ * dot product and normaliser):
+ *     qt_i = phi(q_i), kt_j = phi(k_j) (zero for j >= key_len[b]),
+ *     phi(x) = elu(x) + 1,
+ *     out_i = (sum_{j <= i} (qt_i . kt_j) v_j) / (qt_i . sum_{j <= i} kt_j + eps).
+ *
+ *   q, k     device pointers, fp32 [B, H, N, E] contiguous (the page's
+ *            kernels take float tensors); 4-byte aligned.
+ *   v        device pointer, fp32 [B, H, N, M].
+ *   out      device pointer, fp32 [B, H, N, M], written.
+ *   E, M     feature sizes: multiples of 4 from 4 to 128 (others return
+ *            FATTN_ERR_UNSUPPORTED).
+ *   key_len  device pointer to int32[B] or NULL (all N keys); clamped to
+ *            [0, N].  Query rows are never masked.
+ *   eps      the normaliser's epsilon (the page's default is 1e-6); finite, >= 0.
+ *
+ * The rows are cut into chunks of 64: each chunk's share of the running state
+ * (sum of kt v^T and of kt) is formed, an exclusive prefix over the chunks
+ * gives the state each chunk starts from, and each chunk's outputs combine
+ * its own rows with that state -- the same sums as the page's row-by-row
+ * recurrence, regrouped.  Takes B*H*ceil(N/64)*(E*M + E)*4 bytes of scratch
+ * from the library's pool on `stream`; enqueues three kernels and returns
+ * without synchronising.  Returns FATTN_OK, FATTN_ERR_INVALID_ARG,
+ * FATTN_ERR_UNSUPPORTED or FATTN_ERR_CUDA (argument errors before anything
+ * is enqueued).
+ */
+FATTN_API int fattn_linear_fwd(const float* q, const float* k, const float* v, float* out, int B, int H, int N, int E,
+                               int M, const int32_t* key_len, float eps, void* stream);
+
+/*
  * fattn_set_kernel_events: measurement hook.  While set (non-NULL), every
  * forward or backward call made by the calling thread records `start`
  * (a cudaEvent_t) on its stream just before its dominant kernel and `stop`
  * just after it: the attention kernel of the forward (not the V pre-pass or
  * the split-KV combine; with fattn_fwd_host, around each chunk's, so the last
- * chunk's pair remains) and the dK/dV kernel of the backward.  The events
+ * chunk's pair remains), the dK/dV kernel of the backward, and the output
+ * kernel of fattn_linear_fwd.  The events
  * belong to the caller and must stay valid while set; cudaEventElapsedTime
  * on them then gives that kernel's device time.  NULL, NULL clears the hook.
  * Always returns FATTN_OK.

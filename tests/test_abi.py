@@ -197,3 +197,20 @@ def test_host_entry_point_argument_checks(lib):
     assert hcall(d=100) == binding.FATTN_ERR_UNSUPPORTED
     for name in ("q", "k", "v", "o", "lse"):
         assert hcall(**{name: 0}) == binding.FATTN_ERR_INVALID_ARG, name
+
+
+def lcall(B=1, H=1, N=128, E=64, M=64, eps=1e-6, q=FAKE, k=FAKE, v=FAKE, o=FAKE, kl=None):
+    return binding.linear_raw(q, k, v, o, B, H, N, E, M, kl, eps, None)
+
+
+def test_linear_argument_checks(lib):
+    """fattn_linear_fwd refuses bad arguments before touching the device."""
+    assert lcall(B=0) == binding.FATTN_OK
+    assert lcall(N=-1) == binding.FATTN_ERR_INVALID_ARG
+    assert lcall(eps=-1.0) == binding.FATTN_ERR_INVALID_ARG
+    assert lcall(eps=math.inf) == binding.FATTN_ERR_INVALID_ARG
+    for name in ("q", "k", "v", "o"):
+        assert lcall(**{name: 0}) == binding.FATTN_ERR_INVALID_ARG, name
+    for E, M in ((6, 64), (64, 2), (132, 64), (64, 256), (0, 64)):
+        assert lcall(E=E, M=M) == binding.FATTN_ERR_UNSUPPORTED, (E, M)
+    assert lcall(q=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
