@@ -95,7 +95,7 @@ int configure_d256_kernel() {
 // The linear-attention kernels' shared memory, at the largest feature sizes.
 int configure_linear_kernels() {
   const fattn::LinSmem L(128, 128);
-  const int state_bytes = ((fattn::LIN_C * 129 + 3) / 4 * 4 + fattn::LIN_C * 128) * 4;
+  const int state_bytes = (128 * fattn::LIN_TS + fattn::LIN_C * 128) * 4;
   return cudaFuncSetAttribute(fattn::fattn_linear_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               state_bytes) == cudaSuccess &&
                  cudaFuncSetAttribute(fattn::fattn_linear_output_kernel,
@@ -624,7 +624,8 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   if (!q || !k || !v || !out) return FATTN_ERR_INVALID_ARG;
   if (E < 4 || E > 128 || E % 4 || M < 4 || M > 128 || M % 4) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - fattn::LIN_C) return FATTN_ERR_INVALID_ARG;
-  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4) || (key_len && !aligned(key_len, 4)))
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      (key_len && !aligned(key_len, 4)))
     return FATTN_ERR_INVALID_ARG;
   if (!is_device_pointer(q) || !is_device_pointer(k) || !is_device_pointer(v) || !is_device_pointer(out) ||
       (key_len && !is_device_pointer(key_len)))
@@ -643,8 +644,8 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   const size_t state_floats = (size_t)BH * n_chunks * (size_t)E * M;
   const size_t ksum_floats = (size_t)BH * n_chunks * (size_t)E;
   void* scratch = nullptr;
-  if (cudaMallocFromPoolAsync(&scratch, round_up(state_floats * 4u, 256) + round_up(ksum_floats * 4u, 256), ds->pool,
-                              s) != cudaSuccess) {
+  const size_t t_state = round_up(state_floats * 4u, 256), t_ksum = round_up(ksum_floats * 4u, 256);
+  if (cudaMallocFromPoolAsync(&scratch, 2 * (t_state + t_ksum), ds->pool, s) != cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_CUDA;
   }
@@ -654,8 +655,11 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   p.v = v;
   p.out = out;
   p.key_len = key_len;
-  p.state = reinterpret_cast<float*>(scratch);
-  p.ksum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scratch) + round_up(state_floats * 4u, 256));
+  uint8_t* sb = reinterpret_cast<uint8_t*>(scratch);
+  p.state = reinterpret_cast<float*>(sb);
+  p.ksum = reinterpret_cast<float*>(sb + t_state);
+  p.pstate = reinterpret_cast<float*>(sb + t_state + t_ksum);
+  p.pksum = reinterpret_cast<float*>(sb + 2 * t_state + t_ksum);
   p.B = B;
   p.H = H;
   p.N = N;
@@ -663,7 +667,7 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   p.M = M;
   p.n_chunks = n_chunks;
   p.eps = eps;
-  const int state_smem = ((fattn::LIN_C * (E + 1) + 3) / 4 * 4 + fattn::LIN_C * M) * 4;
+  const int state_smem = (E * fattn::LIN_TS + fattn::LIN_C * M) * 4;
   const int out_smem = fattn::LinSmem(E, M).total * 4;
   fattn::fattn_linear_state_kernel<<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, state_smem, s>>>(p);
   fattn::fattn_linear_scan_kernel<<<(unsigned)(BH * blocks_per_head), fattn::LIN_THREADS, 0, s>>>(p,

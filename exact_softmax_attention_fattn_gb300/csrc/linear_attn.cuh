@@ -11,7 +11,7 @@
 //   1. fattn_linear_state_kernel: per chunk, its share of the state,
 //      sum over its rows of kt_j v_j^T (E x M) and of kt_j (E);
 //   2. fattn_linear_scan_kernel: per head, the exclusive prefix of those
-//      shares over the chunks (the state each chunk starts from), in place;
+//      shares over the chunks (the state each chunk starts from);
 //   3. fattn_linear_output_kernel: per chunk, the rows' numerators
 //      tril(Qt Kt^T) V + Qt S_prefix and denominators
 //      rowsum(tril(Qt Kt^T)) + Qt . s_prefix + eps.
@@ -34,51 +34,110 @@ struct LinParams {
   const float* v;  // [B*H, N, M]
   float* out;      // [B*H, N, M]
   const int32_t* key_len;  // [B] or nullptr
-  float* state;  // [B*H, n_chunks, E*M]: chunk shares, then their exclusive prefix
-  float* ksum;   // [B*H, n_chunks, E]: the same for the key sums
+  float* state;   // [B*H, n_chunks, E*M]: each chunk's share of the state
+  float* ksum;    // [B*H, n_chunks, E]: each chunk's share of the key sum
+  float* pstate;  // [B*H, n_chunks, E*M]: the exclusive prefix of the shares
+  float* pksum;   // [B*H, n_chunks, E]
   int B, H, N, E, M, n_chunks;
   float eps;
 };
 
-__device__ __forceinline__ float lin_phi(float x) { return x > 0.0f ? x + 1.0f : expf(x); }  // elu(x) + 1
+// elu(x) + 1; the fast exponential's error (a few ulp on x <= 0) is far below
+// the fp32 summation error of the sums it feeds
+__device__ __forceinline__ float lin_phi(float x) { return x > 0.0f ? x + 1.0f : __expf(x); }
 
 __device__ __forceinline__ int lin_key_len(const LinParams& p, int bh) {
   int kl = p.key_len ? p.key_len[bh / p.H] : p.N;
   return kl < 0 ? 0 : (kl > p.N ? p.N : kl);
 }
 
+// Row stride (floats) of the transposed [E][LIN_C] arrays: 16-byte aligned
+// rows, offset by 4 banks so the transposing stores conflict at most 4-way.
+constexpr int LIN_TS = LIN_C + 4;
+
 // Shared-memory layout of the output kernel, in floats (every array starts
-// on a 16-byte boundary): Qt, Kt [C][E+1] (padded rows), V [C][M], the
-// prefix state [E][M] and key sum [E], A = tril(Qt Kt^T) [C][C+1], den [C].
+// on a 16-byte boundary): phi(Q)^T and phi(K)^T [E][LIN_TS], V [C][M], the
+// prefix state [E][M] and key sum [E], A^T = tril(Qt Kt^T)^T [C][C], den [C].
 struct LinSmem {
-  int qt, kt, v, ps, pks, a, den, total;
+  int qt, kt, v, ps, pks, at, den, total;
   __host__ __device__ LinSmem(int E, int M) {
     auto up4 = [](int x) { return (x + 3) / 4 * 4; };
     qt = 0;
-    kt = qt + up4(LIN_C * (E + 1));
-    v = kt + up4(LIN_C * (E + 1));
+    kt = qt + E * LIN_TS;
+    v = kt + E * LIN_TS;
     ps = v + up4(LIN_C * M);
     pks = ps + up4(E * M);
-    a = pks + up4(E);
-    den = a + up4(LIN_C * (LIN_C + 1));
-    total = den + up4(LIN_C);
+    at = pks + up4(E);
+    den = at + LIN_C * LIN_C;
+    total = den + LIN_C;
   }
 };
 
-// Loads a chunk's mapped keys (masked rows and rows past N as 0) into
-// kt[C][E+1] and its values (rows past N as 0) into vs[C][M].
-__device__ __forceinline__ void lin_load_kv(const LinParams& p, int bh, int r0, int kl, float* kt, float* vs) {
-  const int E = p.E, M = p.M;
-  for (int idx = threadIdx.x; idx < LIN_C * E; idx += LIN_THREADS) {
-    const int r = idx / E, e = idx % E, row = r0 + r;
-    kt[r * (E + 1) + e] = row < kl ? lin_phi(p.k[((size_t)bh * p.N + row) * E + e]) : 0.0f;
-  }
-  for (int idx = threadIdx.x; idx < LIN_C * M; idx += LIN_THREADS) {
-    const int r = idx / M, m = idx % M, row = r0 + r;
-    vs[r * M + m] = row < p.N ? p.v[((size_t)bh * p.N + row) * M + m] : 0.0f;
+// phi(x) of a chunk's rows (masked rows and rows past N as 0), stored
+// transposed: dst[e * LIN_TS + r].  float4 reads along e (E % 4 == 0), four
+// per thread in flight before any is used.
+__device__ __forceinline__ void lin_load_t(const float* src, int bh, int N, int E, int r0, int lim, float* dst) {
+  const int e4s = E / 4;
+  const int n4 = LIN_C * e4s;
+  for (int base = 0; base < n4; base += 4 * LIN_THREADS) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * LIN_THREADS + threadIdx.x;
+      const int r = idx / e4s, e4 = idx % e4s, row = r0 + r;
+      x[u] = (idx < n4 && row < lim) ? reinterpret_cast<const float4*>(src + ((size_t)bh * N + row) * E)[e4]
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * LIN_THREADS + threadIdx.x;
+      if (idx >= n4) continue;
+      const int r = idx / e4s, e4 = idx % e4s;
+      const bool live = r0 + r < lim;
+      dst[(4 * e4 + 0) * LIN_TS + r] = live ? lin_phi(x[u].x) : 0.0f;
+      dst[(4 * e4 + 1) * LIN_TS + r] = live ? lin_phi(x[u].y) : 0.0f;
+      dst[(4 * e4 + 2) * LIN_TS + r] = live ? lin_phi(x[u].z) : 0.0f;
+      dst[(4 * e4 + 3) * LIN_TS + r] = live ? lin_phi(x[u].w) : 0.0f;
+    }
   }
 }
 
+// dst[0, n_total) <- src[0, n_src) then zeros: float4 copies, four loads
+// per thread in flight before their stores.
+__device__ __forceinline__ void lin_copy4(float4* dst, const float4* __restrict__ src, int n_src, int n_total) {
+  for (int base = 0; base < n_total; base += 4 * LIN_THREADS) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * LIN_THREADS + threadIdx.x;
+      x[u] = idx < n_src ? __ldg(src + idx) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * LIN_THREADS + threadIdx.x;
+      if (idx < n_total) dst[idx] = x[u];
+    }
+  }
+}
+
+// A chunk's value rows (rows past N as 0), row-major [C][M]: the chunk's rows
+// are contiguous in memory.
+__device__ __forceinline__ void lin_load_v(const LinParams& p, int bh, int r0, float* vs) {
+  const int rows = min(LIN_C, p.N - r0);
+  lin_copy4(reinterpret_cast<float4*>(vs),
+            reinterpret_cast<const float4*>(p.v + ((size_t)bh * p.N + r0) * p.M), rows * p.M / 4, LIN_C * p.M / 4);
+}
+
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const float4 b) {
+  const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(av[u], bv[w], acc[u][w]);
+}
+
+// 1. A chunk's share of the state: S_c = phi(K_c)^T V_c (E x M, in 4 x 4
+//    register tiles) and s_c = column sums of phi(K_c).
 __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_state_kernel(const LinParams p) {
   extern __shared__ float4 lin_smem4[];
   float* sm = reinterpret_cast<float*>(lin_smem4);
@@ -86,59 +145,82 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_state_kernel(const L
   const int c = (int)(blockIdx.x % (unsigned)p.n_chunks);
   const int bh = (int)(blockIdx.x / (unsigned)p.n_chunks);
   const int r0 = c * LIN_C;
-  float* kt = sm;
-  float* vs = sm + (LIN_C * (E + 1) + 3) / 4 * 4;
-  lin_load_kv(p, bh, r0, lin_key_len(p, bh), kt, vs);
+  float* kt = sm;                 // [E][LIN_TS]
+  float* vs = sm + E * LIN_TS;    // [C][M]
+  lin_load_t(p.k, bh, p.N, E, r0, lin_key_len(p, bh), kt);
+  lin_load_v(p, bh, r0, vs);
   __syncthreads();
   float* st = p.state + ((size_t)bh * p.n_chunks + c) * (size_t)E * M;
-  // four value columns per item: float4 loads of V rows
-  const int m4s = M / 4;
-  for (int idx = threadIdx.x; idx < E * m4s; idx += LIN_THREADS) {
-    const int e = idx / m4s, m4 = idx % m4s;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const int e4s = E / 4, m4s = M / 4;
+  for (int item = threadIdx.x; item < e4s * m4s; item += LIN_THREADS) {
+    const int e4 = item / m4s, m4 = item % m4s;
+    float acc[4][4] = {};
 #pragma unroll 4
     for (int r = 0; r < LIN_C; ++r) {
-      const float kv = kt[r * (E + 1) + e];
-      const float4 vv = reinterpret_cast<const float4*>(vs + r * M)[m4];
-      acc.x = fmaf(kv, vv.x, acc.x);
-      acc.y = fmaf(kv, vv.y, acc.y);
-      acc.z = fmaf(kv, vv.z, acc.z);
-      acc.w = fmaf(kv, vv.w, acc.w);
+      // phi(K)^T is [E][r]: the four e of this tile at row r are strided; read them
+      const float4 kv = make_float4(kt[(4 * e4) * LIN_TS + r], kt[(4 * e4 + 1) * LIN_TS + r],
+                                    kt[(4 * e4 + 2) * LIN_TS + r], kt[(4 * e4 + 3) * LIN_TS + r]);
+      fma4x4(acc, kv, reinterpret_cast<const float4*>(vs + r * M)[m4]);
     }
-    reinterpret_cast<float4*>(st + (size_t)e * M)[m4] = acc;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      reinterpret_cast<float4*>(st + (size_t)(4 * e4 + u) * M)[m4] =
+          make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
   }
   for (int e = threadIdx.x; e < E; e += LIN_THREADS) {
     float s = 0.0f;
-    for (int r = 0; r < LIN_C; ++r) s += kt[r * (E + 1) + e];
+    const float4* row = reinterpret_cast<const float4*>(kt + e * LIN_TS);
+#pragma unroll 4
+    for (int r4 = 0; r4 < LIN_C / 4; ++r4) {
+      const float4 x = row[r4];
+      s += (x.x + x.y) + (x.z + x.w);
+    }
     p.ksum[((size_t)bh * p.n_chunks + c) * E + e] = s;
   }
 }
 
-// Exclusive prefix over the chunks of one head, in place: one thread per
-// element of the state (and of the key sum), walking the chunks in order.
+// 2. Exclusive prefix over the chunks of one head: one thread per element of
+//    the state (and of the key sum), walking the chunks in order.  Shares and
+//    prefixes are separate arrays, so the loads run ahead of the stores.
 __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_scan_kernel(const LinParams p, int blocks_per_head) {
   const int E = p.E, M = p.M;
   const int bh = (int)(blockIdx.x / (unsigned)blocks_per_head);
   const int idx = (int)(blockIdx.x % (unsigned)blocks_per_head) * LIN_THREADS + threadIdx.x;
   if (idx >= E * M + E) return;
-  float* base;
+  const float* __restrict__ in;
+  float* __restrict__ out;
   size_t stride;
   if (idx < E * M) {
-    base = p.state + (size_t)bh * p.n_chunks * (size_t)E * M + idx;
+    in = p.state + (size_t)bh * p.n_chunks * (size_t)E * M + idx;
+    out = p.pstate + (size_t)bh * p.n_chunks * (size_t)E * M + idx;
     stride = (size_t)E * M;
   } else {
-    base = p.ksum + (size_t)bh * p.n_chunks * (size_t)E + (idx - E * M);
+    in = p.ksum + (size_t)bh * p.n_chunks * (size_t)E + (idx - E * M);
+    out = p.pksum + (size_t)bh * p.n_chunks * (size_t)E + (idx - E * M);
     stride = (size_t)E;
   }
   float run = 0.0f;
-#pragma unroll 8
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const float share = base[c * stride];
-    base[c * stride] = run;
+  int c = 0;
+  for (; c + 16 <= p.n_chunks; c += 16) {  // sixteen loads in flight
+    float sh[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) sh[u] = __ldg(in + (size_t)(c + u) * stride);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      out[(size_t)(c + u) * stride] = run;
+      run += sh[u];
+    }
+  }
+  for (; c < p.n_chunks; ++c) {
+    const float share = __ldg(in + (size_t)c * stride);
+    out[(size_t)c * stride] = run;
     run += share;
   }
 }
 
+// 3. A chunk's outputs: numerators tril(Qt Kt^T) V + Qt S_prefix and
+//    denominators rowsum(tril(Qt Kt^T)) + Qt . s_prefix + eps, all products
+//    in 4 x 4 register tiles fed by float4 shared-memory loads.
 __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_output_kernel(const LinParams p) {
   extern __shared__ float4 lin_smem4[];
   float* sm = reinterpret_cast<float*>(lin_smem4);
@@ -147,66 +229,71 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_output_kernel(const 
   const int c = (int)(blockIdx.x % (unsigned)p.n_chunks);
   const int bh = (int)(blockIdx.x / (unsigned)p.n_chunks);
   const int r0 = c * LIN_C;
-  float *qt = sm + L.qt, *kt = sm + L.kt, *vs = sm + L.v, *ps = sm + L.ps, *pks = sm + L.pks, *a = sm + L.a,
+  float *qt = sm + L.qt, *kt = sm + L.kt, *vs = sm + L.v, *ps = sm + L.ps, *pks = sm + L.pks, *at = sm + L.at,
         *den = sm + L.den;
-  lin_load_kv(p, bh, r0, lin_key_len(p, bh), kt, vs);
-  for (int idx = threadIdx.x; idx < LIN_C * E; idx += LIN_THREADS) {
-    const int r = idx / E, e = idx % E, row = r0 + r;
-    qt[r * (E + 1) + e] = row < p.N ? lin_phi(p.q[((size_t)bh * p.N + row) * E + e]) : 0.0f;
-  }
-  const float* st = p.state + ((size_t)bh * p.n_chunks + c) * (size_t)E * M;
-  for (int idx = threadIdx.x; idx < E * M / 4; idx += LIN_THREADS)
-    reinterpret_cast<float4*>(ps)[idx] = reinterpret_cast<const float4*>(st)[idx];
-  for (int e = threadIdx.x; e < E; e += LIN_THREADS) pks[e] = p.ksum[((size_t)bh * p.n_chunks + c) * E + e];
+  lin_load_t(p.q, bh, p.N, E, r0, p.N, qt);
+  lin_load_t(p.k, bh, p.N, E, r0, lin_key_len(p, bh), kt);
+  lin_load_v(p, bh, r0, vs);
+  const float* st = p.pstate + ((size_t)bh * p.n_chunks + c) * (size_t)E * M;
+  lin_copy4(reinterpret_cast<float4*>(ps), reinterpret_cast<const float4*>(st), E * M / 4, E * M / 4);
+  for (int e = threadIdx.x; e < E; e += LIN_THREADS) pks[e] = p.pksum[((size_t)bh * p.n_chunks + c) * E + e];
   __syncthreads();
-  // A = tril(Qt Kt^T): the chunk's own rows j <= i
-  for (int idx = threadIdx.x; idx < LIN_C * LIN_C; idx += LIN_THREADS) {
-    const int i = idx / LIN_C, j = idx % LIN_C;
-    float s = 0.0f;
-    if (j <= i) {
+  // A = tril(Qt Kt^T), stored transposed (at[j][i]); 16 x 16 tiles of 4 x 4
+  {
+    const int ti = threadIdx.x / 16, tj = threadIdx.x % 16;  // rows 4ti.., columns 4tj..
+    float acc[4][4] = {};
+    if (tj <= ti) {
 #pragma unroll 4
-      for (int e = 0; e < E; ++e) s = fmaf(qt[i * (E + 1) + e], kt[j * (E + 1) + e], s);
+      for (int e = 0; e < E; ++e)
+        fma4x4(acc, reinterpret_cast<const float4*>(qt + e * LIN_TS)[ti],
+               reinterpret_cast<const float4*>(kt + e * LIN_TS)[tj]);
     }
-    a[i * (LIN_C + 1) + j] = s;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {  // column j = 4tj + w of A is row j of A^T
+      const int j = 4 * tj + w;
+      float4 col;
+      col.x = j <= 4 * ti + 0 ? acc[0][w] : 0.0f;
+      col.y = j <= 4 * ti + 1 ? acc[1][w] : 0.0f;
+      col.z = j <= 4 * ti + 2 ? acc[2][w] : 0.0f;
+      col.w = j <= 4 * ti + 3 ? acc[3][w] : 0.0f;
+      reinterpret_cast<float4*>(at + j * LIN_C)[ti] = col;
+    }
   }
   __syncthreads();
-  // denominators: the chunk's own keys (row sums of A) and those before it
-  for (int i = threadIdx.x; i < LIN_C; i += LIN_THREADS) {
-    float d = p.eps;
-    for (int j = 0; j <= i; ++j) d += a[i * (LIN_C + 1) + j];
-    for (int e = 0; e < E; ++e) d = fmaf(qt[i * (E + 1) + e], pks[e], d);
-    den[i] = d;
+  // denominators: the chunk's own keys (row sums of A) and those before it;
+  // four adjacent lanes per row, each a quarter of the terms
+  {
+    static_assert(LIN_THREADS == 4 * LIN_C, "four threads per row");
+    const int i = threadIdx.x / 4, part = threadIdx.x % 4;
+    float d = 0.0f;
+    for (int j = part; j <= i; j += 4) d += at[j * LIN_C + i];
+    for (int e = part; e < E; e += 4) d = fmaf(qt[e * LIN_TS + i], pks[e], d);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    if (part == 0) den[i] = d + p.eps;
   }
   __syncthreads();
-  // numerators, four value columns per item, divided by the row's denominator
+  // numerators in 4 x 4 tiles (rows 4ti.., value columns 4tc..), divided by den
   const int m4s = M / 4;
-  for (int idx = threadIdx.x; idx < LIN_C * m4s; idx += LIN_THREADS) {
-    const int i = idx / m4s, m4 = idx % m4s, row = r0 + i;
-    if (row >= p.N) continue;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int j = 0; j <= i; ++j) {
-      const float w = a[i * (LIN_C + 1) + j];
-      const float4 vv = reinterpret_cast<const float4*>(vs + j * M)[m4];
-      acc.x = fmaf(w, vv.x, acc.x);
-      acc.y = fmaf(w, vv.y, acc.y);
-      acc.z = fmaf(w, vv.z, acc.z);
-      acc.w = fmaf(w, vv.w, acc.w);
-    }
+  for (int item = threadIdx.x; item < (LIN_C / 4) * m4s; item += LIN_THREADS) {
+    const int ti = item / m4s, tc = item % m4s;
+    float acc[4][4] = {};
+    const int jmax = 4 * ti + 4;  // A is zero past the tile's last row
 #pragma unroll 4
-    for (int e = 0; e < E; ++e) {
-      const float w = qt[i * (E + 1) + e];
-      const float4 sv = reinterpret_cast<const float4*>(ps + e * M)[m4];
-      acc.x = fmaf(w, sv.x, acc.x);
-      acc.y = fmaf(w, sv.y, acc.y);
-      acc.z = fmaf(w, sv.z, acc.z);
-      acc.w = fmaf(w, sv.w, acc.w);
+    for (int j = 0; j < jmax; ++j)
+      fma4x4(acc, reinterpret_cast<const float4*>(at + j * LIN_C)[ti], reinterpret_cast<const float4*>(vs + j * M)[tc]);
+#pragma unroll 4
+    for (int e = 0; e < E; ++e)
+      fma4x4(acc, reinterpret_cast<const float4*>(qt + e * LIN_TS)[ti],
+             reinterpret_cast<const float4*>(ps + e * M)[tc]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int row = r0 + 4 * ti + u;
+      if (row >= p.N) continue;
+      const float inv = 1.0f / den[4 * ti + u];
+      reinterpret_cast<float4*>(p.out + ((size_t)bh * p.N + row) * M)[tc] =
+          make_float4(acc[u][0] * inv, acc[u][1] * inv, acc[u][2] * inv, acc[u][3] * inv);
     }
-    const float inv = 1.0f / den[i];
-    float* o = p.out + ((size_t)bh * p.N + row) * M + 4 * m4;
-    o[0] = acc.x * inv;
-    o[1] = acc.y * inv;
-    o[2] = acc.z * inv;
-    o[3] = acc.w * inv;
   }
 }
 

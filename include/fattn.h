@@ -207,9 +207,9 @@ FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, i
  *     out_i = (sum_{j <= i} (qt_i . kt_j) v_j) / (qt_i . sum_{j <= i} kt_j + eps).
  *
  *   q, k     device pointers, fp32 [B, H, N, E] contiguous (the page's
- *            kernels take float tensors); 4-byte aligned.
- *   v        device pointer, fp32 [B, H, N, M].
- *   out      device pointer, fp32 [B, H, N, M], written.
+ *            kernels take float tensors); 16-byte aligned.
+ *   v        device pointer, fp32 [B, H, N, M]; 16-byte aligned.
+ *   out      device pointer, fp32 [B, H, N, M], written; 16-byte aligned.
  *   E, M     feature sizes: multiples of 4 from 4 to 128 (others return
  *            FATTN_ERR_UNSUPPORTED).
  *   key_len  device pointer to int32[B] or NULL (all N keys); clamped to
@@ -220,7 +220,7 @@ FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, i
  * (sum of kt v^T and of kt) is formed, an exclusive prefix over the chunks
  * gives the state each chunk starts from, and each chunk's outputs combine
  * its own rows with that state -- the same sums as the page's row-by-row
- * recurrence, regrouped.  Takes B*H*ceil(N/64)*(E*M + E)*4 bytes of scratch
+ * recurrence, regrouped.  Takes 2*B*H*ceil(N/64)*(E*M + E)*4 bytes of scratch
  * from the library's pool on `stream`; enqueues three kernels and returns
  * without synchronising.  Returns FATTN_OK, FATTN_ERR_INVALID_ARG,
  * FATTN_ERR_UNSUPPORTED or FATTN_ERR_CUDA (argument errors before anything

@@ -214,3 +214,6 @@ def test_linear_argument_checks(lib):
     for E, M in ((6, 64), (64, 2), (132, 64), (64, 256), (0, 64)):
         assert lcall(E=E, M=M) == binding.FATTN_ERR_UNSUPPORTED, (E, M)
     assert lcall(q=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
+    assert lcall(k=FAKE + 4) == binding.FATTN_ERR_INVALID_ARG
+    assert lcall(v=FAKE + 4) == binding.FATTN_ERR_INVALID_ARG  # float4 rows
+    assert lcall(o=FAKE + 8) == binding.FATTN_ERR_INVALID_ARG
