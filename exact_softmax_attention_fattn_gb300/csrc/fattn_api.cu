@@ -95,7 +95,7 @@ int configure_d256_kernel() {
 // The linear-attention kernels' shared memory, at the largest feature sizes.
 int configure_linear_kernels() {
   const fattn::LinSmem L(128, 128);
-  const int state_bytes = (128 * fattn::LIN_TS + fattn::LIN_C * 128) * 4;
+  const int state_bytes = (128 * fattn::LIN_C + fattn::LIN_C * 128) * 4;
   return cudaFuncSetAttribute(fattn::fattn_linear_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               state_bytes) == cudaSuccess &&
                  cudaFuncSetAttribute(fattn::fattn_linear_output_kernel,
@@ -667,7 +667,7 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   p.M = M;
   p.n_chunks = n_chunks;
   p.eps = eps;
-  const int state_smem = (E * fattn::LIN_TS + fattn::LIN_C * M) * 4;
+  const int state_smem = (E * fattn::LIN_C + fattn::LIN_C * M) * 4;
   const int out_smem = fattn::LinSmem(E, M).total * 4;
   fattn::fattn_linear_state_kernel<<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, state_smem, s>>>(p);
   fattn::fattn_linear_scan_kernel<<<(unsigned)(BH * blocks_per_head), fattn::LIN_THREADS, 0, s>>>(p,

@@ -51,53 +51,61 @@ __device__ __forceinline__ int lin_key_len(const LinParams& p, int bh) {
   return kl < 0 ? 0 : (kl > p.N ? p.N : kl);
 }
 
-// Row stride (floats) of the transposed [E][LIN_C] arrays: 16-byte aligned
-// rows, offset by 4 banks so the transposing stores conflict at most 4-way.
-constexpr int LIN_TS = LIN_C + 4;
+// The transposed [E][LIN_C] arrays (phi(Q)^T, phi(K)^T) and A^T [LIN_C][LIN_C]
+// are stored unpadded, each row's sixteen float4 groups permuted: group g of
+// row e sits in slot g ^ ((e >> 2) & 15).  A warp that writes four rows r of
+// eight consecutive e4 (the load below) and a warp that writes A^T rows of
+// many (ti, tj) pairs then spread over all 32 banks, while every reader still
+// gets whole float4 groups.
+__device__ __forceinline__ int lin_slot(int e, int g) { return g ^ ((e >> 2) & 15); }
+__device__ __forceinline__ int lin_at(int e, int r) { return e * LIN_C + 4 * lin_slot(e, r >> 2) + (r & 3); }
 
 // Shared-memory layout of the output kernel, in floats (every array starts
-// on a 16-byte boundary): phi(Q)^T and phi(K)^T [E][LIN_TS], V [C][M], the
-// prefix state [E][M] and key sum [E], A^T = tril(Qt Kt^T)^T [C][C], den [C].
+// on a 16-byte boundary): phi(Q)^T [E][C]; phi(K)^T [E][C], whose space A^T =
+// tril(Qt Kt^T)^T [C][C] takes over once A is formed; V [C][M]; the prefix
+// state [E][M] and key sum [E]; den [C].
 struct LinSmem {
-  int qt, kt, v, ps, pks, at, den, total;
+  int qt, kt, at, v, ps, pks, den, total;
   __host__ __device__ LinSmem(int E, int M) {
     auto up4 = [](int x) { return (x + 3) / 4 * 4; };
     qt = 0;
-    kt = qt + E * LIN_TS;
-    v = kt + E * LIN_TS;
+    kt = at = qt + E * LIN_C;
+    v = kt + (E > LIN_C ? E : LIN_C) * LIN_C;
     ps = v + up4(LIN_C * M);
     pks = ps + up4(E * M);
-    at = pks + up4(E);
-    den = at + LIN_C * LIN_C;
+    den = pks + up4(E);
     total = den + LIN_C;
   }
 };
 
 // phi(x) of a chunk's rows (masked rows and rows past N as 0), stored
-// transposed: dst[e * LIN_TS + r].  float4 reads along e (E % 4 == 0), four
-// per thread in flight before any is used.
+// transposed and permuted: element (e, r) at lin_at(e, r).  Each warp reads
+// four rows, eight float4 (128 bytes) of each; each thread keeps four loads
+// in flight before any is used.
 __device__ __forceinline__ void lin_load_t(const float* src, int bh, int N, int E, int r0, int lim, float* dst) {
   const int e4s = E / 4;
-  const int n4 = LIN_C * e4s;
-  for (int base = 0; base < n4; base += 4 * LIN_THREADS) {
+  const int n = (LIN_C / 4) * ((e4s + 7) / 8) * 32;  // (row quads) x (e4 octets) x lanes
+  for (int base = 0; base < n; base += 4 * LIN_THREADS) {
     float4 x[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int idx = base + u * LIN_THREADS + threadIdx.x;
-      const int r = idx / e4s, e4 = idx % e4s, row = r0 + r;
-      x[u] = (idx < n4 && row < lim) ? reinterpret_cast<const float4*>(src + ((size_t)bh * N + row) * E)[e4]
-                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const int idx = base + u * LIN_THREADS + threadIdx.x, lane = idx & 31, rest = idx >> 5;
+      const int r = 4 * (rest % (LIN_C / 4)) + (lane & 3), e4 = 8 * (rest / (LIN_C / 4)) + (lane >> 2);
+      const int row = r0 + r;
+      x[u] = (idx < n && e4 < e4s && row < lim)
+                 ? reinterpret_cast<const float4*>(src + ((size_t)bh * N + row) * E)[e4]
+                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int idx = base + u * LIN_THREADS + threadIdx.x;
-      if (idx >= n4) continue;
-      const int r = idx / e4s, e4 = idx % e4s;
+      const int idx = base + u * LIN_THREADS + threadIdx.x, lane = idx & 31, rest = idx >> 5;
+      const int r = 4 * (rest % (LIN_C / 4)) + (lane & 3), e4 = 8 * (rest / (LIN_C / 4)) + (lane >> 2);
+      if (idx >= n || e4 >= e4s) continue;
       const bool live = r0 + r < lim;
-      dst[(4 * e4 + 0) * LIN_TS + r] = live ? lin_phi(x[u].x) : 0.0f;
-      dst[(4 * e4 + 1) * LIN_TS + r] = live ? lin_phi(x[u].y) : 0.0f;
-      dst[(4 * e4 + 2) * LIN_TS + r] = live ? lin_phi(x[u].z) : 0.0f;
-      dst[(4 * e4 + 3) * LIN_TS + r] = live ? lin_phi(x[u].w) : 0.0f;
+      dst[lin_at(4 * e4 + 0, r)] = live ? lin_phi(x[u].x) : 0.0f;
+      dst[lin_at(4 * e4 + 1, r)] = live ? lin_phi(x[u].y) : 0.0f;
+      dst[lin_at(4 * e4 + 2, r)] = live ? lin_phi(x[u].z) : 0.0f;
+      dst[lin_at(4 * e4 + 3, r)] = live ? lin_phi(x[u].w) : 0.0f;
     }
   }
 }
@@ -137,7 +145,8 @@ __device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const
 }
 
 // 1. A chunk's share of the state: S_c = phi(K_c)^T V_c (E x M, in 4 x 4
-//    register tiles) and s_c = column sums of phi(K_c).
+//    register tiles, four rows of the chunk per step: four float4 of phi(K)^T
+//    and four of V feed 64 FMAs) and s_c = column sums of phi(K_c).
 __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_state_kernel(const LinParams p) {
   extern __shared__ float4 lin_smem4[];
   float* sm = reinterpret_cast<float*>(lin_smem4);
@@ -145,8 +154,8 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_state_kernel(const L
   const int c = (int)(blockIdx.x % (unsigned)p.n_chunks);
   const int bh = (int)(blockIdx.x / (unsigned)p.n_chunks);
   const int r0 = c * LIN_C;
-  float* kt = sm;                 // [E][LIN_TS]
-  float* vs = sm + E * LIN_TS;    // [C][M]
+  float* kt = sm;                 // [E][C], permuted
+  float* vs = sm + E * LIN_C;     // [C][M]
   lin_load_t(p.k, bh, p.N, E, r0, lin_key_len(p, bh), kt);
   lin_load_v(p, bh, r0, vs);
   __syncthreads();
@@ -154,13 +163,17 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_state_kernel(const L
   const int e4s = E / 4, m4s = M / 4;
   for (int item = threadIdx.x; item < e4s * m4s; item += LIN_THREADS) {
     const int e4 = item / m4s, m4 = item % m4s;
+    const float4* k4 = reinterpret_cast<const float4*>(kt + 4 * e4 * LIN_C);  // rows 4e4.. share one permutation
     float acc[4][4] = {};
-#pragma unroll 4
-    for (int r = 0; r < LIN_C; ++r) {
-      // phi(K)^T is [E][r]: the four e of this tile at row r are strided; read them
-      const float4 kv = make_float4(kt[(4 * e4) * LIN_TS + r], kt[(4 * e4 + 1) * LIN_TS + r],
-                                    kt[(4 * e4 + 2) * LIN_TS + r], kt[(4 * e4 + 3) * LIN_TS + r]);
-      fma4x4(acc, kv, reinterpret_cast<const float4*>(vs + r * M)[m4]);
+#pragma unroll 2
+    for (int g = 0; g < LIN_C / 4; ++g) {
+      const int sl = lin_slot(4 * e4, g);
+      const float4 k0 = k4[sl], k1 = k4[LIN_C / 4 + sl], k2 = k4[LIN_C / 2 + sl], k3 = k4[3 * LIN_C / 4 + sl];
+      const float4* v4 = reinterpret_cast<const float4*>(vs + 4 * g * M) + m4;
+      fma4x4(acc, make_float4(k0.x, k1.x, k2.x, k3.x), v4[0]);
+      fma4x4(acc, make_float4(k0.y, k1.y, k2.y, k3.y), v4[m4s]);
+      fma4x4(acc, make_float4(k0.z, k1.z, k2.z, k3.z), v4[2 * m4s]);
+      fma4x4(acc, make_float4(k0.w, k1.w, k2.w, k3.w), v4[3 * m4s]);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -169,10 +182,10 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_state_kernel(const L
   }
   for (int e = threadIdx.x; e < E; e += LIN_THREADS) {
     float s = 0.0f;
-    const float4* row = reinterpret_cast<const float4*>(kt + e * LIN_TS);
+    const float4* row = reinterpret_cast<const float4*>(kt + e * LIN_C);
 #pragma unroll 4
-    for (int r4 = 0; r4 < LIN_C / 4; ++r4) {
-      const float4 x = row[r4];
+    for (int g = 0; g < LIN_C / 4; ++g) {
+      const float4 x = row[lin_slot(e, g)];
       s += (x.x + x.y) + (x.z + x.w);
     }
     p.ksum[((size_t)bh * p.n_chunks + c) * E + e] = s;
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_output_kernel(const 
   const int c = (int)(blockIdx.x % (unsigned)p.n_chunks);
   const int bh = (int)(blockIdx.x / (unsigned)p.n_chunks);
   const int r0 = c * LIN_C;
-  float *qt = sm + L.qt, *kt = sm + L.kt, *vs = sm + L.v, *ps = sm + L.ps, *pks = sm + L.pks, *at = sm + L.at,
+  float *qt = sm + L.qt, *kt = sm + L.kt, *at = sm + L.at, *vs = sm + L.v, *ps = sm + L.ps, *pks = sm + L.pks,
         *den = sm + L.den;
   lin_load_t(p.q, bh, p.N, E, r0, p.N, qt);
   lin_load_t(p.k, bh, p.N, E, r0, lin_key_len(p, bh), kt);
@@ -238,36 +251,47 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_output_kernel(const 
   lin_copy4(reinterpret_cast<float4*>(ps), reinterpret_cast<const float4*>(st), E * M / 4, E * M / 4);
   for (int e = threadIdx.x; e < E; e += LIN_THREADS) pks[e] = p.pksum[((size_t)bh * p.n_chunks + c) * E + e];
   __syncthreads();
-  // A = tril(Qt Kt^T), stored transposed (at[j][i]); 16 x 16 tiles of 4 x 4
+  // A = tril(Qt Kt^T): only its 136 4 x 4 tiles on or below the diagonal,
+  // one per thread (tile t -> row ti, column tj <= ti); then, once every
+  // thread is done with phi(K)^T, stored transposed (A^T row j = column j of
+  // A) over it
   {
-    const int ti = threadIdx.x / 16, tj = threadIdx.x % 16;  // rows 4ti.., columns 4tj..
+    constexpr int NT = LIN_C / 4, N_TRI = NT * (NT + 1) / 2;
+    static_assert(N_TRI <= LIN_THREADS, "one tile per thread");
+    int ti = 0, tj = threadIdx.x;
+    while (tj > ti) tj -= ++ti;  // tj - ti(ti+1)/2 after the loop
     float acc[4][4] = {};
-    if (tj <= ti) {
+    if (threadIdx.x < N_TRI) {
 #pragma unroll 4
       for (int e = 0; e < E; ++e)
-        fma4x4(acc, reinterpret_cast<const float4*>(qt + e * LIN_TS)[ti],
-               reinterpret_cast<const float4*>(kt + e * LIN_TS)[tj]);
+        fma4x4(acc, reinterpret_cast<const float4*>(qt + e * LIN_C)[lin_slot(e, ti)],
+               reinterpret_cast<const float4*>(kt + e * LIN_C)[lin_slot(e, tj)]);
     }
+    __syncthreads();
+    if (threadIdx.x < N_TRI) {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {  // column j = 4tj + w of A is row j of A^T
-      const int j = 4 * tj + w;
-      float4 col;
-      col.x = j <= 4 * ti + 0 ? acc[0][w] : 0.0f;
-      col.y = j <= 4 * ti + 1 ? acc[1][w] : 0.0f;
-      col.z = j <= 4 * ti + 2 ? acc[2][w] : 0.0f;
-      col.w = j <= 4 * ti + 3 ? acc[3][w] : 0.0f;
-      reinterpret_cast<float4*>(at + j * LIN_C)[ti] = col;
+      for (int w = 0; w < 4; ++w) {
+        const int j = 4 * tj + w;
+        float4 col;
+        col.x = j <= 4 * ti + 0 ? acc[0][w] : 0.0f;
+        col.y = j <= 4 * ti + 1 ? acc[1][w] : 0.0f;
+        col.z = j <= 4 * ti + 2 ? acc[2][w] : 0.0f;
+        col.w = j <= 4 * ti + 3 ? acc[3][w] : 0.0f;
+        reinterpret_cast<float4*>(at + j * LIN_C)[lin_slot(j, ti)] = col;
+      }
     }
   }
   __syncthreads();
-  // denominators: the chunk's own keys (row sums of A) and those before it;
-  // four adjacent lanes per row, each a quarter of the terms
+  // denominators: the chunk's own keys (row sums of A, whose tiles above the
+  // diagonal were never stored: the loop stops at j = i) and those before
+  // it; four adjacent lanes per row, each a quarter of the terms, in blocks
   {
     static_assert(LIN_THREADS == 4 * LIN_C, "four threads per row");
     const int i = threadIdx.x / 4, part = threadIdx.x % 4;
     float d = 0.0f;
-    for (int j = part; j <= i; j += 4) d += at[j * LIN_C + i];
-    for (int e = part; e < E; e += 4) d = fmaf(qt[e * LIN_TS + i], pks[e], d);
+    for (int j = part * (LIN_C / 4); j < (part + 1) * (LIN_C / 4) && j <= i; ++j) d += at[lin_at(j, i)];
+    const int eq = E / 4;
+    for (int e = part * eq; e < (part + 1) * eq; ++e) d = fmaf(qt[lin_at(e, i)], pks[e], d);
     d += __shfl_xor_sync(0xffffffffu, d, 1);
     d += __shfl_xor_sync(0xffffffffu, d, 2);
     if (part == 0) den[i] = d + p.eps;
@@ -281,10 +305,11 @@ __global__ void __launch_bounds__(LIN_THREADS) fattn_linear_output_kernel(const 
     const int jmax = 4 * ti + 4;  // A is zero past the tile's last row
 #pragma unroll 4
     for (int j = 0; j < jmax; ++j)
-      fma4x4(acc, reinterpret_cast<const float4*>(at + j * LIN_C)[ti], reinterpret_cast<const float4*>(vs + j * M)[tc]);
+      fma4x4(acc, reinterpret_cast<const float4*>(at + j * LIN_C)[lin_slot(j, ti)],
+             reinterpret_cast<const float4*>(vs + j * M)[tc]);
 #pragma unroll 4
     for (int e = 0; e < E; ++e)
-      fma4x4(acc, reinterpret_cast<const float4*>(qt + e * LIN_TS)[ti],
+      fma4x4(acc, reinterpret_cast<const float4*>(qt + e * LIN_C)[lin_slot(e, ti)],
              reinterpret_cast<const float4*>(ps + e * M)[tc]);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
