@@ -96,10 +96,13 @@ int configure_d256_kernel() {
 int configure_linear_kernels() {
   const fattn::LinSmem L(128, 128);
   const int state_bytes = (128 * fattn::LIN_C + fattn::LIN_C * 128) * 4;
-  return cudaFuncSetAttribute(fattn::fattn_linear_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              state_bytes) == cudaSuccess &&
-                 cudaFuncSetAttribute(fattn::fattn_linear_output_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, L.total * 4) == cudaSuccess
+  const fattn::LinSmem L64(64, 64);
+  const int state64 = (64 * fattn::LIN_C + fattn::LIN_C * 64) * 4;
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  return cudaFuncSetAttribute(fattn::fattn_linear_state_kernel<0, 0>, attr, state_bytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_linear_output_kernel<0, 0>, attr, L.total * 4) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_linear_state_kernel<64, 64>, attr, state64) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_linear_output_kernel<64, 64>, attr, L64.total * 4) == cudaSuccess
              ? FATTN_OK
              : FATTN_ERR_CUDA;
 }
@@ -669,11 +672,18 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   p.eps = eps;
   const int state_smem = (E * fattn::LIN_C + fattn::LIN_C * M) * 4;
   const int out_smem = fattn::LinSmem(E, M).total * 4;
-  fattn::fattn_linear_state_kernel<<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, state_smem, s>>>(p);
+  const bool f64 = E == 64 && M == 64;  // the sizes compiled as constants
+  if (f64)
+    fattn::fattn_linear_state_kernel<64, 64><<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, state_smem, s>>>(p);
+  else
+    fattn::fattn_linear_state_kernel<0, 0><<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, state_smem, s>>>(p);
   fattn::fattn_linear_scan_kernel<<<(unsigned)(BH * blocks_per_head), fattn::LIN_THREADS, 0, s>>>(p,
                                                                                                    blocks_per_head);
   mark_kernel_start(s);
-  fattn::fattn_linear_output_kernel<<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, out_smem, s>>>(p);
+  if (f64)
+    fattn::fattn_linear_output_kernel<64, 64><<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, out_smem, s>>>(p);
+  else
+    fattn::fattn_linear_output_kernel<0, 0><<<(unsigned)(BH * n_chunks), fattn::LIN_THREADS, out_smem, s>>>(p);
   mark_kernel_stop(s);
   if (cudaGetLastError() != cudaSuccess) rc = FATTN_ERR_CUDA;
   if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
