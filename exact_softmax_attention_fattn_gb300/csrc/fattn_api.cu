@@ -50,12 +50,12 @@ void mark_kernel_stop(cudaStream_t s) {
   if (t_kernel_stop) cudaEventRecord(t_kernel_stop, s);
 }
 EncodeTiledFn g_encode = nullptr;
-unsigned long long g_wait_limit_ns = 0;
 
 // Limit of every bounded wait inside the kernel: 2 s unless FATTN_WAIT_LIMIT_MS
-// or (finer, taking precedence) FATTN_WAIT_LIMIT_US is set; read once.
+// or (finer, taking precedence) FATTN_WAIT_LIMIT_US is set; read once (the
+// static's initialisation is thread-safe).
 unsigned long long wait_limit_ns() {
-  if (g_wait_limit_ns == 0) {
+  static const unsigned long long limit = [] {
     unsigned long long ns = 2000ull * 1000000ull;
     if (const char* e = std::getenv("FATTN_WAIT_LIMIT_MS")) {
       long long v = std::atoll(e);
@@ -65,9 +65,9 @@ unsigned long long wait_limit_ns() {
       long long v = std::atoll(e);
       if (v > 0) ns = (unsigned long long)v * 1000ull;
     }
-    g_wait_limit_ns = ns;
-  }
-  return g_wait_limit_ns;
+    return ns;
+  }();
+  return limit;
 }
 
 // Sets the kernel's shared-memory limit and checks that it was compiled with
@@ -130,13 +130,20 @@ int make_pool(int dev, cudaMemPool_t* pool) {
   props.handleTypes = cudaMemHandleTypeNone;
   props.location.type = cudaMemLocationTypeDevice;
   props.location.id = dev;
-  if (cudaMemPoolCreate(pool, &props) != cudaSuccess) return FATTN_ERR_CUDA;
+  cudaMemPool_t made = nullptr;
+  if (cudaMemPoolCreate(&made, &props) != cudaSuccess) return FATTN_ERR_CUDA;
   uint64_t keep = UINT64_MAX;
-  if (cudaMemPoolSetAttribute(*pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaMemPoolSetAttribute(made, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+    cudaMemPoolDestroy(made);
+    return FATTN_ERR_CUDA;
+  }
+  *pool = made;  // set only once the pool is complete
   return FATTN_OK;
 }
 
-// Per-device set-up, once: SM count, kernel attributes, the error word.
+// Per-device set-up, once: SM count, kernel attributes, the error word.  A
+// set-up that failed part of the way is resumed by the next call: resources
+// already made are kept, not made again.
 int device_state(int dev, DeviceState** out) {
   if (dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -159,11 +166,19 @@ int device_state(int dev, DeviceState** out) {
     if (rc == FATTN_OK) rc = configure_d256_kernel<false>();
     if (rc == FATTN_OK) rc = configure_linear_kernels();
     if (rc != FATTN_OK) return rc;
-    if (make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
-    if (cudaMalloc(&s.err, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
-    if (cudaStreamCreateWithFlags(&s.copy_in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&s.copy_out, cudaStreamNonBlocking) != cudaSuccess)
+    if (!s.pool && make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
+    if (!s.err && cudaMalloc(&s.err, 4 * sizeof(int)) != cudaSuccess) {
+      s.err = nullptr;
       return FATTN_ERR_CUDA;
+    }
+    if (!s.copy_in && cudaStreamCreateWithFlags(&s.copy_in, cudaStreamNonBlocking) != cudaSuccess) {
+      s.copy_in = nullptr;
+      return FATTN_ERR_CUDA;
+    }
+    if (!s.copy_out && cudaStreamCreateWithFlags(&s.copy_out, cudaStreamNonBlocking) != cudaSuccess) {
+      s.copy_out = nullptr;
+      return FATTN_ERR_CUDA;
+    }
     if (cudaMemset(s.err, 0, 4 * sizeof(int)) != cudaSuccess) return FATTN_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return FATTN_ERR_CUDA;
     s.ready = true;
