@@ -68,12 +68,14 @@ CSRC = os.path.join(ROOT, "exact_softmax_attention_fattn_gb300", "csrc")
 
 
 KERNEL_SOURCES = ("fattn_kernel.cuh", "ptx.cuh")
+BWD_SOURCES = ("fattn_bwd.cuh", "ptx.cuh")
+LINEAR_SOURCES = ("linear_attn.cuh",)
 
 
-def kernel_source_hash() -> str:
-    """Hash of the attention kernel's own source (not the host launcher)."""
+def kernel_source_hash(sources: tuple[str, ...] = KERNEL_SOURCES) -> str:
+    """Hash of a kernel's own source files (not the host launcher)."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -89,10 +91,13 @@ def measured_peaks() -> tuple[float, str, float | None]:
         return FALLBACK_BF16_TFLOPS, "fallback", 6800.0
 
 
-def ncu_traffic(workload: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if it was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.txt")
+def ncu_traffic(workload: str, profile: str | None = None, sources: tuple[str, ...] = KERNEL_SOURCES,
+                field: str = "dram_bytes_per_launch") -> float | None:
+    """DRAM bytes per launch of the dominant kernel from its committed ncu
+    summary (profiles/<profile>.txt, default the attention kernel's for this
+    workload), if the summary was taken on the current kernel source (its
+    kernel_source_hash line matches); else None."""
+    path = os.path.join(ROOT, "profiles", f"{profile or KERNEL_NAME + '_' + workload}.txt")
     try:
         fields = {}
         with open(path) as f:
@@ -100,10 +105,10 @@ def ncu_traffic(workload: str) -> float | None:
                 if ":" in line:
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        if fields.get("kernel_source_hash") != kernel_source_hash():
+        if fields.get("kernel_source_hash", "").split()[:1] != [kernel_source_hash(sources)]:
             return None
-        return float(fields["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        return float(fields[field].split()[0])
+    except (OSError, KeyError, ValueError, IndexError):
         return None
 
 
@@ -513,7 +518,9 @@ def linear_arm(args, rank: int, world: int, local_rank: int):
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                      "peak_kind": "fp32 CUDA-core FMA peak derived from SMs x 128 lanes x 2 x max SM clock",
-                     "traffic": None, "kernel": "fattn_linear_output_kernel alone", "kernel_ms_mean": out_mean},
+                     "traffic": ncu_traffic(name, f"fattn_linear_kernels_{name}", LINEAR_SOURCES,
+                                            "output_dram_bytes_per_launch"),
+                     "kernel": "fattn_linear_output_kernel alone", "kernel_ms_mean": out_mean},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # chunk state, scan, output
@@ -629,7 +636,9 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
                    "causal": w.causal, "key_padding": x.key_len is not None, "flops_per_step": flops,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}", "traffic": None,
+                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
+                     "traffic": ncu_traffic(args.workload, f"fattn_bwd_kernels_{args.workload}", BWD_SOURCES,
+                                            "dkdv_dram_bytes_per_launch"),
                      "kernel": "dK/dV kernel alone (its 4 GEMMs: 2x the forward's FLOPs)",
                      "kernel_ms_mean": dkdv_mean_ms},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
