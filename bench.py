@@ -46,6 +46,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -72,12 +73,21 @@ BWD_SOURCES = ("fattn_bwd.cuh", "ptx.cuh")
 LINEAR_SOURCES = ("linear_attn.cuh",)
 
 
+def code_only(text: str) -> str:
+    """C++ source without its comments, trailing blanks and empty lines: what
+    decides the compiled kernel (string literals here hold no comment marks)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash(sources: tuple[str, ...] = KERNEL_SOURCES) -> str:
-    """Hash of a kernel's own source files (not the host launcher)."""
+    """Hash of a kernel's own source code (not the host launcher), comments
+    excluded, so that a capture stays valid across comment edits only."""
     h = hashlib.sha256()
     for name in sources:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

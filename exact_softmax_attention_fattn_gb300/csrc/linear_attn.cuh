@@ -20,8 +20,11 @@
 // constants (every shared-memory offset an immediate) and for any other
 // sizes at run time (template arguments 0).
 // fp32 throughout, as the page's float kernels, on the CUDA cores: the
-// chunk products are small (64 x 64 x E) and the data move is what bounds
-// the problem at the feature sizes the page dispatches on.
+// chunk products are small (64 x 64 x E at the feature sizes the page
+// dispatches on), and rounding the operands to tf32 for the tensor cores
+// would cost more accuracy than the fp32 sums.  The state and output kernels
+// are bound by instruction issue (the FFMA products, their shared-memory
+// operand loads and the transform of phi), not by HBM.
 #pragma once
 
 #include <cstdint>
@@ -67,7 +70,7 @@ __device__ __forceinline__ int lin_at(int e, int r) { return e * LIN_C + 4 * lin
 // on a 16-byte boundary): phi(Q)^T [E][C]; phi(K)^T [E][C], whose space A^T =
 // tril(Qt Kt^T)^T [C][C] takes over once A is formed; X, which holds the
 // prefix state [E][M] for the Qt S_prefix products and then V [C][M] for the
-// A V products; the prefix key sum [E]; den [C].
+// A V products; the prefix key sum [E]; 1 / den for each row [C].
 struct LinSmem {
   int qt, kt, at, x, pks, den, total;
   __host__ __device__ LinSmem(int E, int M) {
