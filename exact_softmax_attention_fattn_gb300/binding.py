@@ -22,8 +22,8 @@ FATTN_ERR_UNSUPPORTED = 2
 FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
-EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_splitkv_plan", "fattn_bwd",
-            "fattn_linear_fwd", "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error",
+EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_fwd_noalloc", "fattn_splitkv_plan",
+            "fattn_bwd", "fattn_linear_fwd", "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error",
             "fattn_version")
 
 _lock = threading.Lock()
@@ -69,6 +69,8 @@ def load_library():
             ]
             lib.fattn_fwd_host.restype = ctypes.c_int
             lib.fattn_fwd_host.argtypes = lib.fattn_fwd.argtypes
+            lib.fattn_fwd_noalloc.restype = ctypes.c_int
+            lib.fattn_fwd_noalloc.argtypes = lib.fattn_fwd.argtypes
             lib.fattn_linear_fwd.restype = ctypes.c_int
             lib.fattn_linear_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [
                 ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]
@@ -110,6 +112,14 @@ def fwd_host_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
     """fattn_fwd_host with raw HOST addresses; returns the status code."""
     return load_library().fattn_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
                                          float(scale), int(bool(causal)), key_len_ptr, stream)
+
+
+def noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int, N: int, d: int,
+                scale: float, causal: bool, key_len_ptr: int | None, stream: int | None) -> int:
+    """fattn_fwd_noalloc (the forward on the library's static scratch, never
+    split) with raw device addresses; returns the status code."""
+    return load_library().fattn_fwd_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N), int(d),
+                                            float(scale), int(bool(causal)), key_len_ptr, stream)
 
 
 def linear_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, B: int, H: int, N: int, E: int, M: int,

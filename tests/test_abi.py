@@ -217,3 +217,27 @@ def test_linear_argument_checks(lib):
     assert lcall(k=FAKE + 4) == binding.FATTN_ERR_INVALID_ARG
     assert lcall(v=FAKE + 4) == binding.FATTN_ERR_INVALID_ARG  # float4 rows
     assert lcall(o=FAKE + 8) == binding.FATTN_ERR_INVALID_ARG
+
+
+def test_binding_types_every_entry_point(lib):
+    """The binding lists, and gives argument types to, every entry point the
+    header declares."""
+    assert set(binding.EXPORTED) == set(declared_symbols())
+    for name in binding.EXPORTED:
+        assert getattr(lib, name).argtypes is not None, name  # ctypes leaves it None unless set
+
+
+def test_noalloc_validates_like_fattn_fwd(lib):
+    """fattn_fwd_noalloc through the binding: the same host-side checks as
+    fattn_fwd, before anything touches the device."""
+    def na(B=1, H=1, N=128, d=64, scale=0.125, q=FAKE, o=FAKE, lse=FAKE):
+        return binding.noalloc_raw(q, FAKE, FAKE, o, lse, B, H, N, d, scale, False, None, None)
+
+    assert na(B=0) == binding.FATTN_OK
+    assert na(B=-1) == binding.FATTN_ERR_INVALID_ARG
+    assert na(scale=math.nan) == binding.FATTN_ERR_INVALID_ARG
+    assert na(q=0) == binding.FATTN_ERR_INVALID_ARG
+    assert na(d=60) == binding.FATTN_ERR_UNSUPPORTED
+    assert na(q=FAKE + 8) == binding.FATTN_ERR_INVALID_ARG  # not 16-byte aligned
+    # beyond the static scratch: B*H*N*d*2 bytes of V copy alone exceed 64 MiB
+    assert na(B=64, H=16, N=4096, d=128) == binding.FATTN_ERR_UNSUPPORTED
