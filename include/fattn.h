@@ -41,7 +41,7 @@ extern "C" {
 typedef enum {
   FATTN_OK = 0,
   FATTN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or scale is invalid */
-  FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration this build runs (head dim) */
+  FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration the library runs (head dim) */
   FATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FATTN_ERR_TIMEOUT = 4      /* a bounded wait inside the kernel gave up (see fattn_last_error) */
 } fattn_status;
@@ -268,7 +268,7 @@ FATTN_API int fattn_last_error(void* stream, int* detail);
  * memory: code that runs where neither cudaMalloc nor a stream-ordered pool
  * may be used, for instance inside a host framework that owns all device
  * memory through its own arena, or a real-time path that must not take the
- * driver's allocation locks.  The paper has no counterpart; this is a
+ * driver's allocation locks.  The pages have no counterpart; this is a
  * property of the library, not of the method.
  *
  * Arguments, layouts, semantics and results are exactly those of fattn_fwd,
