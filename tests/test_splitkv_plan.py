@@ -68,6 +68,16 @@ def test_low_occupancy_shapes_split(lib, B, H, N, causal):
     assert 2 <= n <= 16
 
 
+def test_short_causal_shape_keeps_one_split(lib):
+    """B4 H8 N1024 causal: 128 query blocks of at most 8 key tiles.  Splitting
+    would give 256 or more units for 152 CTAs, so each CTA still walks as many
+    key-tile steps and pays one more fixed per-unit cost; measured on a GB300
+    (2 and 4 forced splits 103 and 82 TFLOP/s against 126 unsplit), and the
+    plan agrees."""
+    assert units(4, 8, 1024) < 152
+    assert binding.splitkv_plan(4, 8, 1024, True, 152, 0) == 1
+
+
 def test_more_sms_never_fewer_splits(lib):
     """32 query blocks of 64 key tiles: more SMs can only help by splitting more."""
     prev = 1
