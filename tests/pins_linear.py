@@ -91,9 +91,44 @@ def lin_first_row_closed_form(orc):
     assert np.max(np.abs(out[:, :, 0] - want)) <= 1e-12, "first row differs from its closed form"
 
 
+def lin_chunked_regrouping(orc):
+    """The regrouping the GPU kernels compute, restated in numpy: the rows cut
+    into chunks of C; per chunk, tril(phi(Q_c) phi(K_c)^T) V_c plus phi(Q_c)
+    times the state of all earlier chunks, over the row sums of the same
+    lower triangle plus phi(Q_c) . (earlier key sums) + eps; then the chunk's
+    own share (phi(K_c)^T V_c, column sums of phi(K_c)) joins the state.  The
+    same sums as the running state, regrouped: equal to rounding for any C,
+    including chunks cut across the key-length mask and a ragged last chunk."""
+    for N, E, M, kl, C in ((130, 8, 6, [100], 64), (37, 4, 5, None, 5), (9, 3, 2, [4, 9], 1),
+                           (200, 16, 8, [150, 200], 64)):
+        B = 1 if kl is None else len(kl)
+        q, k, v = _inputs(B, 2, N, E, M, 200 + N)
+        eps = 1e-3
+        ours = orc.linear(q, k, v, key_len=kl, eps=eps)
+        qt, kt, vv = _phi(q), _phi(k), v.astype(np.float64)
+        if kl is not None:
+            mask = (np.arange(N)[None, :] < np.asarray(kl)[:, None]).astype(np.float64)
+            kt = kt * mask[:, None, :, None]
+        ref = np.zeros(vv.shape)
+        state = np.zeros((B, 2, E, M))
+        ksum = np.zeros((B, 2, E))
+        for c0 in range(0, N, C):
+            c1 = min(N, c0 + C)
+            qc, kc, vc = qt[:, :, c0:c1], kt[:, :, c0:c1], vv[:, :, c0:c1]
+            a = np.einsum("bhie,bhje->bhij", qc, kc) * np.tril(np.ones((c1 - c0, c1 - c0)))
+            num = np.einsum("bhij,bhjm->bhim", a, vc) + np.einsum("bhie,bhem->bhim", qc, state)
+            den = a.sum(axis=3) + np.einsum("bhie,bhe->bhi", qc, ksum) + eps
+            ref[:, :, c0:c1] = num / den[..., None]
+            state = state + np.einsum("bhje,bhjm->bhem", kc, vc)
+            ksum = ksum + kc.sum(axis=2)
+        err = np.max(np.abs(ours - ref)) / max(1.0, np.max(np.abs(ref)))
+        assert err <= 1e-12, f"chunked form differs by {err:.3g} (N={N}, C={C}, key_len={kl})"
+
+
 ALL_PINS = [
     ("quadratic_form", lin_matches_quadratic_form),
     ("feature_map_values", lin_feature_map_values),
     ("masks_and_invariants", lin_masks_and_invariants),
     ("first_row_closed_form", lin_first_row_closed_form),
+    ("chunked_regrouping", lin_chunked_regrouping),
 ]
