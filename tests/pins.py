@@ -255,6 +255,34 @@ def pin_masked_keys_irrelevant(orc):
     np.testing.assert_array_equal(l1[1, :, :6], l2[1, :, :6])
 
 
+def pin_block_merge(orc):
+    """Merging the final states of key blocks, as the split-KV combine does:
+    for a partition of the keys into blocks, each block's normalised output
+    O_t and log-sum-exp L_t (the oracle on that block alone: its keys and
+    values moved to the front, the rest masked by key_len) give the whole
+    result as L = log sum_t e^(L_t), O = sum_t e^(L_t - L) O_t
+    ("understand-flashattention", complete derivation for two blocks, applied
+    to the blocks' final statistics)."""
+    B, H, N, d = 1, 2, 50, 16
+    x = make_inputs(Workload("bm", B, H, N, d, False, 35, qk_sigma=2.0))
+    sc = 0.3
+    o, lse = orc.forward(x.q, x.k, x.v, sc, False)
+    for cuts in ([1], [17], [49], [10, 30], [5, 6, 40]):
+        edges = [0] + cuts + [N]
+        outs, lses = [], []
+        for s, e in zip(edges[:-1], edges[1:]):
+            kb, vb = np.zeros_like(x.k), np.zeros_like(x.v)
+            kb[:, :, : e - s] = x.k[:, :, s:e]
+            vb[:, :, : e - s] = x.v[:, :, s:e]
+            ob, lb = orc.forward(x.q, kb, vb, sc, False, key_len=np.full(B, e - s, np.int32))
+            outs.append(np.asarray(ob, np.float64))
+            lses.append(np.asarray(lb, np.float64))
+        big_l = np.logaddexp.reduce(np.stack(lses), axis=0)
+        big_o = sum(np.exp(lt - big_l)[..., None] * ot for lt, ot in zip(lses, outs))
+        np.testing.assert_allclose(big_o, o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(big_l, lse, rtol=1e-12, atol=0)
+
+
 ALL_PINS = [
     ("n1", pin_n1),
     ("n2_logistic", pin_n2_logistic),
@@ -272,4 +300,5 @@ ALL_PINS = [
     ("brute", pin_brute),
     ("fully_masked", pin_fully_masked),
     ("masked_keys_irrelevant", pin_masked_keys_irrelevant),
+    ("block_merge", pin_block_merge),
 ]

@@ -71,6 +71,10 @@ def test_torch_fp64_cross_check(causal, use_kl):
     pins.pin_torch(oracle, causal, use_kl)
 
 
+def test_key_blocks_merge_to_the_whole():
+    pins.pin_block_merge(oracle)
+
+
 def test_brute_force_tiny():
     pins.pin_brute(oracle)
 
