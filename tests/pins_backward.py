@@ -127,9 +127,41 @@ def bwd_constant_v_and_zero_scale(orc):
     assert np.max(np.abs(dv - expect)) <= 1e-12, "scale-0 dV is not the uniform average"
 
 
+def bwd_row_term_from_output(orc):
+    """The reformulation the GPU kernels use: P recomputed from the forward's
+    log-sum-exp (P = exp(S - LSE), "recomputing P needs logsumexp") and the
+    row term of dS taken as D_i = dO_i . O_i instead of sum_k dP_ik P_ik
+    (equal, since O_i = sum_k P_ik V_k).  A numpy backward built that way from
+    the oracle's own forward O and LSE equals the oracle's backward."""
+    for causal, key_len in ((True, None), (False, [90, 41]), (True, [77, 0])):
+        x, g = _inputs(2, 2, 90, 16, causal, 71)
+        scale = 0.3
+        o, lse = orc.forward(x.q, x.k, x.v, scale, causal, key_len=key_len)
+        dq, dk, dv = orc.backward(x.q, x.k, x.v, g, scale, causal, key_len=key_len)
+        q, k, v, go = (_f64(a) for a in (x.q, x.k, x.v, g))
+        N = q.shape[2]
+        vis = np.ones((2, 1, N, N), dtype=bool)
+        if causal:
+            vis &= np.tril(np.ones((N, N), dtype=bool))[None, None]
+        if key_len is not None:
+            vis &= np.arange(N)[None, None, None, :] < np.asarray(key_len)[:, None, None, None]
+        s = scale * np.einsum("bhid,bhjd->bhij", q, k)
+        finite = np.isfinite(lse)  # rows with a visible key
+        lse0 = np.where(finite, lse, 0.0)[..., None]
+        p = np.where(vis & finite[..., None], np.exp(np.where(vis, s, 0.0) - lse0), 0.0)
+        row = np.einsum("bhim,bhim->bhi", go, o)
+        ds = p * (np.einsum("bhim,bhjm->bhij", go, v) - row[..., None])
+        ref = (scale * np.einsum("bhij,bhjd->bhid", ds, k), scale * np.einsum("bhij,bhid->bhjd", ds, q),
+               np.einsum("bhij,bhim->bhjm", p, go))
+        for name, ours, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            err = np.max(np.abs(ours - want)) / max(1.0, np.max(np.abs(want)))
+            assert err <= 1e-10, f"{name} from the output-based row term differs by {err:.3g}"
+
+
 ALL_PINS = [
     ("torch_autograd", bwd_matches_torch_autograd),
     ("finite_differences", bwd_matches_finite_differences),
     ("invariants", bwd_invariants),
     ("constant_v_zero_scale", bwd_constant_v_and_zero_scale),
+    ("row_term_from_output", bwd_row_term_from_output),
 ]
