@@ -86,3 +86,27 @@ def test_golden(name):
         np.testing.assert_allclose(o[0, 0, r], [float.fromhex(t) for t in row], rtol=0, atol=1e-12)
     # values are bf16-exact in fp32
     assert np.all(bf16_bits_to_f32(x.q).view(np.uint32) & 0xFFFF == 0)
+
+
+def test_linear_workload_recipe():
+    """The linear-attention workloads: fp32 N(0, 1) Q, K, V of the stated
+    shapes from their own seeds, key lengths in range, deterministic, and the
+    FLOP count the bench reports (the recurrence's 4 E M + 4 E per row)."""
+    from exact_softmax_attention_fattn_gb300.inputs import LINEAR_WORKLOADS, linear_flops, make_linear_inputs
+
+    w = LINEAR_WORKLOADS["lin_b2h16n4096e64"]
+    assert (w.B, w.H, w.N, w.E, w.M, w.seed, w.key_len_range) == (2, 16, 4096, 64, 64, 8, None)
+    assert linear_flops(w) == 2 * 16 * 4096 * (4 * 64 * 64 + 4 * 64) == 2181038080
+    wk = LINEAR_WORKLOADS["lin_b8h8n2048e64_keylen"]
+    assert (wk.B, wk.H, wk.N, wk.E, wk.M, wk.seed, wk.key_len_range) == (8, 8, 2048, 64, 64, 9, (1024, 2048))
+    small = wk.__class__("t", 8, 2, 64, 8, 4, 9, key_len_range=(1024, 2048))
+    x1, x2 = make_linear_inputs(small), make_linear_inputs(small)
+    assert x1.q.dtype == np.float32 and x1.q.shape == (8, 2, 64, 8) and x1.v.shape == (8, 2, 64, 4)
+    np.testing.assert_array_equal(x1.q, x2.q)
+    np.testing.assert_array_equal(x1.v, x2.v)
+    assert x1.key_len.dtype == np.int32 and np.all((x1.key_len >= 1024) & (x1.key_len <= 2048))
+    np.testing.assert_array_equal(x1.key_len, x2.key_len)
+    big = make_linear_inputs(w.__class__("m", 1, 1, 4096, 64, 64, 8))
+    z = big.q.astype(np.float64)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+    assert not np.array_equal(big.q, big.k)  # Q and K from separate streams
