@@ -1,11 +1,12 @@
 """Attention-forward benchmark: one JSON line on rank 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--pass fwd|bwd|linear] [--splits K]
 
-A step is one exact attention forward (the whole fused kernel: tile loads,
-scores, masks, online softmax, correction, PV, epilogue) over the workload's
-synthetic inputs, already resident in HBM.  Between timed steps the L2 cache
+A step is one exact attention forward over the workload's synthetic inputs,
+already resident in HBM: the V pre-pass and the fused attention kernel (tile
+loads, scores, masks, online softmax, correction, PV, epilogue), plus the
+split-KV combine when the key range is split.  Between timed steps the L2 cache
 is flushed by writing a 256 MiB buffer; each step's kernel is timed with CUDA
 events on the stream it is launched on, and the steps' times are summed.
 nvidia-smi samples the clocks from the start of the warm-up, which runs the
@@ -29,10 +30,18 @@ workload, in the same metric.
 forward's O and LSE, which are computed once before the timed region), with
 FLOPs counted as 2.5x the forward's (five GEMMs of the forward's size).
 
+--pass linear times causal linear attention (fattn_linear_fwd: chunk state,
+prefix scan, output kernels) on the linear workloads (--workload lin_...),
+in TFLOP/s of the page's recurrence (4*E*M + 4*E per row), its roofline the
+fp32 CUDA-core FMA peak.
+
 roofline.achieved is the dominant kernel's rate on its own device time: the
 library records two CUDA events around it on its stream
 (fattn_set_kernel_events) -- the attention kernel of the forward, the dK/dV
-kernel of the backward -- while `value` covers the whole step.
+kernel of the backward, the output kernel of linear attention -- while
+`value` covers the whole step.  roofline.traffic is that kernel's DRAM bytes
+per launch from its committed ncu summary (profiles/), reported only while
+the summary's kernel_source_hash matches the kernel's current code.
 
 The forward splits each query block's key range (split-KV, with a combine
 kernel) when the library's plan says so -- on shapes with fewer blocks of 256
