@@ -39,7 +39,14 @@ roofline.achieved is the dominant kernel's rate on its own device time: the
 library records two CUDA events around it on its stream
 (fattn_set_kernel_events) -- the attention kernel of the forward, the dK/dV
 kernel of the backward, the output kernel of linear attention -- while
-`value` covers the whole step.  roofline.traffic is that kernel's DRAM bytes
+`value` covers the whole step.  The forward's roofline has two legs, tensor
+(algorithmic FLOPs at the measured bf16 burst peak) and HBM (algorithmic bytes
+at the measured copy bandwidth); `bound` names the one whose time at peak is
+longer, and roofline.frac / kernel_frac_of_peak / step_frac_of_peak are that
+roof's fractions for the kernel alone and for the whole step.  The tensor rate
+against the clock-derived peak (SMs x 8192 FLOP/clk x the sampled SM clock)
+and the tensor-pipe activity of the committed ncu summary are reported beside
+it.  roofline.traffic is that kernel's DRAM bytes
 per launch from its committed ncu summary (profiles/), reported only while
 the summary's kernel_source_hash matches the kernel's current code.
 
@@ -67,19 +74,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from exact_softmax_attention_fattn_gb300.inputs import (  # noqa: E402
-    HEADLINE, LINEAR_WORKLOADS, WORKLOADS, causal_flops, make_inputs)
+    HEADLINE, LINEAR_WORKLOADS, WORKLOADS, algorithmic_bytes, causal_flops, make_inputs)
 
 KERNEL_NAME = "fattn_fwd_kernel"
 METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 bf16 dense peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+# Dense bf16 tensor-core rate of one SM per clock (a 128x128x16 MMA every 64
+# cycles): the clock-derived peak is SMs x this x the sampled SM clock.
+TENSOR_FLOP_PER_CLK_SM = 8192.0
 CSRC = os.path.join(ROOT, "exact_softmax_attention_fattn_gb300", "csrc")
 
 
 KERNEL_SOURCES = ("fattn_kernel.cuh", "ptx.cuh")
 BWD_SOURCES = ("fattn_bwd.cuh", "ptx.cuh")
-LINEAR_SOURCES = ("linear_attn.cuh",)
+LINEAR_SOURCES = ("linear_tc.cuh", "ptx.cuh")
 
 
 def code_only(text: str) -> str:
@@ -105,9 +116,60 @@ def measured_peaks() -> tuple[float, str, float | None]:
     try:
         with open(path) as f:
             pk = json.load(f)
-        return float(pk["bf16_tflops"]), "measured", float(pk.get("hbm_gbs")) if pk.get("hbm_gbs") else None
+        hbm = float(pk["hbm_gbs"]) if pk.get("hbm_gbs") else FALLBACK_HBM_GBS
+        return float(pk["bf16_tflops"]), "measured", hbm
     except (OSError, KeyError, ValueError):
-        return FALLBACK_BF16_TFLOPS, "fallback", 6800.0
+        return FALLBACK_BF16_TFLOPS, "fallback", FALLBACK_HBM_GBS
+
+
+def profile_field(profile: str, field: str, sources: tuple[str, ...] = KERNEL_SOURCES) -> str | None:
+    """A field of a committed ncu summary (profiles/<profile>.txt), only while
+    the summary's kernel_source_hash matches the current kernel source."""
+    try:
+        fields = {}
+        with open(os.path.join(ROOT, "profiles", profile + ".txt")) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_hash", "").split()[:1] != [kernel_source_hash(sources)]:
+            return None
+        return fields.get(field)
+    except OSError:
+        return None
+
+
+def forward_roofline(flops: float, nbytes: float, kernel_ms: float, step_ms: float, peak_tf: float,
+                     peak_kind: str, hbm_gbs: float, sm_mhz: float | None, sms: int) -> dict:
+    """Both roofs of one forward: tensor (algorithmic FLOPs at the measured
+    bf16 peak) and HBM (algorithmic bytes at the measured copy bandwidth).
+    `bound` is the roof with the longer time at peak; `achieved`, `peak` and
+    `frac` are that roof's, on the dominant kernel's own CUDA-event time.
+    The other roof, the whole step's fractions and the tensor fraction of the
+    clock-derived peak (SMs x 8192 FLOP/clk x the sampled SM clock) follow."""
+    t_tensor = flops / (peak_tf * 1e12)
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    tensor = {"achieved": flops / (kernel_ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+              "peak_kind": f"bf16 dense burst, {peak_kind}"}
+    tensor["frac"] = tensor["achieved"] / peak_tf
+    tensor["step_frac"] = flops / (step_ms * 1e-3) / 1e12 / peak_tf
+    hbm = {"achieved": nbytes / (kernel_ms * 1e-3) / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+           "peak_kind": f"copy bandwidth, {peak_kind}", "algorithmic_bytes": nbytes}
+    hbm["frac"] = hbm["achieved"] / hbm_gbs
+    hbm["step_frac"] = nbytes / (step_ms * 1e-3) / 1e9 / hbm_gbs
+    bound, other = ("tensor", "hbm") if t_tensor >= t_hbm else ("hbm", "tensor")
+    legs = {"tensor": tensor, "hbm": hbm}
+    out = {"bound": bound}
+    out.update({k: legs[bound][k] for k in ("achieved", "peak", "unit", "frac", "peak_kind")})
+    out["kernel_frac_of_peak"] = legs[bound]["frac"]
+    out["step_frac_of_peak"] = legs[bound]["step_frac"]
+    out[other] = legs[other]
+    out["time_at_peak_us"] = {"tensor": t_tensor * 1e6, "hbm": t_hbm * 1e6}
+    if sm_mhz:
+        clock_peak = sms * TENSOR_FLOP_PER_CLK_SM * sm_mhz * 1e6 / 1e12
+        out["tensor_frac_of_clock_peak"] = tensor["achieved"] / clock_peak
+        out["clock_peak_tflops"] = clock_peak
+    return out
 
 
 def ncu_traffic(workload: str, profile: str | None = None, sources: tuple[str, ...] = KERNEL_SOURCES,
@@ -278,11 +340,15 @@ def reference_arm(args, rank: int, world: int):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": flops_step / (value * 1e12) * 1e3 if value > 0 else None,
+        # measured: the oracle's seconds per timed step (one bounded sample of rows)
+        "ms_per_step": secs / max(1, args.steps) * 1e3,
+        # not measured: the whole workload's time at the sampled rate
+        "projected_ms_full_workload": flops_step / (value * 1e12) * 1e3 if value > 0 else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64/Box-Muller, bf16-rounded)",
         "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-                   "sample": "bounded random query rows per step (oracle on host cores)"},
+                   "sample": "bounded random query rows per step (oracle on host cores)",
+                   "rows_per_step": rows_tot / max(1, args.steps)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -390,11 +456,18 @@ def our_arm(args, rank: int, world: int, local_rank: int):
 
     if rank != 0:
         return
-    peak, peak_kind, _ = measured_peaks()
+    peak, peak_kind, hbm_gbs = measured_peaks()
     # the dominant kernel (the attention kernel) on its own CUDA-event time
     attn_mean_ms = float(np.mean(attn_ms))
-    achieved = flops / (attn_mean_ms * 1e-3) / 1e12
     traffic = ncu_traffic(args.workload)
+    roof = forward_roofline(flops, algorithmic_bytes(w, x.key_len), attn_mean_ms, ms_per_step, peak, peak_kind,
+                            hbm_gbs, (clocks or {}).get("sm_mhz"), sms)
+    roof.update({"traffic": traffic if n_splits == 1 else None,
+                 "kernel": "attention kernel alone (V pre-pass and split-KV combine excluded)",
+                 "kernel_ms_mean": attn_mean_ms})
+    tpa = profile_field(KERNEL_NAME + "_" + args.workload, "tensor_pipe_active_pct_of_active")
+    if tpa:
+        roof["ncu_tensor_pipe_active_pct"] = float(tpa.split()[0])
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v_cpu, rows, dt, threads, desc = oracle_sample(args.workload, args.cpu_seconds, x)
@@ -410,12 +483,10 @@ def our_arm(args, rank: int, world: int, local_rank: int):
                    "key_padding": x.key_len is not None, "flops_per_step": flops,
                    "kv_splits": n_splits, "kv_split_choice": "library" if args.splits is None else "forced",
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "traffic": traffic if n_splits == 1 else None,
-                     "kernel": "attention kernel alone (V pre-pass and split-KV combine excluded)",
-                     "kernel_ms_mean": attn_mean_ms},
-        "pct_of_bf16_peak": 100.0 * (flops / (ms_per_step * 1e-3) / 1e12) / peak,
+        "roofline": roof,
+        # the whole call (every kernel of the step) against the same roof as roofline.frac
+        "kernel_frac_of_peak": roof["kernel_frac_of_peak"],
+        "step_frac_of_peak": roof["step_frac_of_peak"],
         "clocks": clocks,
         "e2e": e2e,
         # V pre-pass + attention kernel per step, + the split-KV combine when split
@@ -428,12 +499,22 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     print(json.dumps(line), flush=True)
 
 
+def linear_parts(B: int, H: int, N: int, sms: int) -> int:
+    """Parts per head of the tensor-core linear attention (feature sizes up
+    to 64), as the library cuts them: about one CTA per SM over all heads."""
+    n_tiles = -(-N // 128)
+    n_parts = max(1, min(n_tiles, sms // max(1, B * H)))
+    tpp = -(-n_tiles // n_parts)
+    return -(-n_tiles // tpp)
+
+
 def linear_arm(args, rank: int, world: int, local_rank: int):
     """--pass linear: causal linear attention (fattn_linear_fwd, fp32) on one
     of LINEAR_WORKLOADS, timed like the forward; FLOPs are the page's
-    recurrence (linear_flops); the roofline is the output kernel's, against the
-    fp32 CUDA-core peak (152 SMs x 128 lanes x 2 FLOP x the sampled max SM
-    clock), since these kernels run on the CUDA cores."""
+    recurrence (linear_flops).  At feature sizes up to 64 it runs on the
+    tensor cores (a part-totals launch when a head is cut into parts, then the
+    output launch); the roofline is the output kernel's, with the HBM leg
+    (Q, K, V read and the output written once, in fp32) and the tensor leg."""
     import torch
     import torch.distributed as dist
 
@@ -514,11 +595,18 @@ def linear_arm(args, rank: int, world: int, local_rank: int):
                "ms_per_step": e2e_s * 1e3}
     if rank != 0:
         return
-    sm_max = (clocks or {}).get("sm_max_mhz") or 2070.0
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    peak = sms * 128 * 2 * sm_max * 1e6 / 1e12  # fp32 FMA lanes x 2 FLOP x clock
     out_mean = float(np.mean(out_ms))
-    achieved = flops / (out_mean * 1e-3) / 1e12
+    n_parts = linear_parts(w.B, w.H, w.N, sms)
+    nbytes = float(w.B * w.H * w.N) * (2 * w.E + 2 * w.M) * 4
+    peak_tf, peak_kind, hbm_gbs = measured_peaks()
+    roof = forward_roofline(flops, nbytes, out_mean, ms_per_step, peak_tf, peak_kind, hbm_gbs,
+                            (clocks or {}).get("sm_mhz"), sms)
+    roof.update({"traffic": ncu_traffic(name, f"fattn_linear_kernels_{name}", LINEAR_SOURCES,
+                                        "output_dram_bytes_per_launch"),
+                 "kernel": "fattn_linear_tc_kernel (output launch) alone", "kernel_ms_mean": out_mean,
+                 "flops_counted": "the recurrence's 4*E*M + 4*E per row (the tensor cores run three bf16 "
+                                  "terms of each chunked product)"})
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         t0 = time.perf_counter()
@@ -535,15 +623,15 @@ def linear_arm(args, rank: int, world: int, local_rank: int):
         "config": {"workload": name, "pass": "linear", "B": w.B, "H": w.H, "N": w.N, "E": w.E, "M": w.M,
                    "key_padding": x.key_len is not None, "flops_per_step": flops,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                     "peak_kind": "fp32 CUDA-core FMA peak derived from SMs x 128 lanes x 2 x max SM clock",
-                     "traffic": ncu_traffic(name, f"fattn_linear_kernels_{name}", LINEAR_SOURCES,
-                                            "output_dram_bytes_per_launch"),
-                     "kernel": "fattn_linear_output_kernel alone", "kernel_ms_mean": out_mean},
+        "roofline": roof,
+        "kernel_frac_of_peak": roof["kernel_frac_of_peak"],
+        "step_frac_of_peak": roof["step_frac_of_peak"],
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,  # chunk state, scan, output
-        "kernel": "fattn_linear_state_kernel + fattn_linear_scan_kernel + fattn_linear_output_kernel",
+        # part totals (when a head is cut into parts) + output
+        "gpu_launches": (1 + (n_parts > 1)) * args.steps,
+        "kernel": "fattn_linear_tc_kernel<STATE> + fattn_linear_tc_kernel<OUTPUT>",
+        "config_parts_per_head": n_parts,
         "kernel_ms": {"min": min(step_ms), "median": float(np.median(step_ms)), "max": max(step_ms)},
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,

@@ -16,6 +16,7 @@
 #include "fattn_d256.cuh"
 #include "fattn_kernel.cuh"
 #include "linear_attn.cuh"
+#include "linear_tc.cuh"
 #include "splitkv_combine.cuh"
 #include "v_prepass.cuh"
 
@@ -99,7 +100,10 @@ int configure_linear_kernels() {
   const fattn::LinSmem L64(64, 64);
   const int state64 = (64 * fattn::LIN_C + fattn::LIN_C * 64) * 4;
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  return cudaFuncSetAttribute(fattn::fattn_linear_state_kernel<0, 0>, attr, state_bytes) == cudaSuccess &&
+  const int tc_bytes = (int)fattn::LtcCfg::SMEM_BYTES;
+  return cudaFuncSetAttribute(fattn::fattn_linear_tc_kernel<true>, attr, tc_bytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_linear_tc_kernel<false>, attr, tc_bytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_linear_state_kernel<0, 0>, attr, state_bytes) == cudaSuccess &&
                  cudaFuncSetAttribute(fattn::fattn_linear_output_kernel<0, 0>, attr, L.total * 4) == cudaSuccess &&
                  cudaFuncSetAttribute(fattn::fattn_linear_state_kernel<64, 64>, attr, state64) == cudaSuccess &&
                  cudaFuncSetAttribute(fattn::fattn_linear_output_kernel<64, 64>, attr, L64.total * 4) == cudaSuccess
@@ -213,6 +217,20 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// [B*H, N, F] fp32 viewed as a 3-D tensor {F, N, B*H}, boxes of 64 x 128 x 1
+// without swizzle (rows of 256 bytes in shared memory); columns past F and
+// rows past N read as zero.
+int encode_map_f32(CUtensorMap* map, const void* ptr, int BH, int N, int F) {
+  cuuint64_t dims[3] = {(cuuint64_t)F, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)F * 4ull, (cuuint64_t)N * (cuuint64_t)F * 4ull};
+  cuuint32_t box[3] = {(cuuint32_t)fattn::LTC_F, (cuuint32_t)fattn::LTC_T, 1u};
+  cuuint32_t elem[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+}
 
 // Head dims the kernels run: multiples of 8 (rows of 16-byte vectors, TMA
 // strides in 16-byte units), computed in the 64-, 128- or 256-column kernel
@@ -434,6 +452,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
   if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
+  if (d > 128 && splits_requested > 1) return FATTN_ERR_UNSUPPORTED;  // no split-KV above 128 columns
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       (key_len && !aligned(key_len, 4)))
@@ -463,7 +482,6 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.causal = causal ? 1 : 0;
   p.n_qblocks = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
   p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
-  if (d > 128 && splits_requested > 1) return FATTN_ERR_UNSUPPORTED;  // no split-KV above 128 columns
   p.n_splits = d > 128 ? 1 : plan_splits(B, H, N, p.causal, ds->num_sms, splits_requested);
   const long long units = (long long)B * H * p.n_qblocks * p.n_splits;
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
@@ -659,6 +677,52 @@ extern "C" FATTN_API int fattn_linear_fwd(const float* q, const float* k, const 
   int rc = device_state(dev, &ds);
   if (rc != FATTN_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (E <= fattn::LTC_F && M <= fattn::LTC_F) {
+    // tensor cores: parts of whole 128-row tiles, about one CTA per SM in all
+    const int n_tiles = (N + fattn::LTC_T - 1) / fattn::LTC_T;
+    int n_parts = (int)std::max(1ll, std::min<long long>(n_tiles, ds->num_sms / std::max(1ll, BH)));
+    const int tpp = (n_tiles + n_parts - 1) / n_parts;
+    n_parts = (n_tiles + tpp - 1) / tpp;
+    if (BH * n_parts > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
+    fattn::LtcParams lp;
+    lp.out = out;
+    lp.key_len = key_len;
+    lp.tot = nullptr;
+    lp.err = ds->err;
+    lp.B = B;
+    lp.H = H;
+    lp.N = N;
+    lp.E = E;
+    lp.M = M;
+    lp.n_parts = n_parts;
+    lp.tiles_per_part = tpp;
+    lp.tot_stride = (int)round_up((size_t)(E * M + E), 4);
+    lp.eps = eps;
+    lp.wait_limit_ns = wait_limit_ns();
+    CUtensorMap mq, mk, mv;
+    if (encode_map_f32(&mq, q, (int)BH, N, E) != FATTN_OK || encode_map_f32(&mk, k, (int)BH, N, E) != FATTN_OK ||
+        encode_map_f32(&mv, v, (int)BH, N, M) != FATTN_OK)
+      return FATTN_ERR_CUDA;
+    void* tot = nullptr;
+    if (n_parts > 1) {
+      // each part's totals, written by the state launch and read by the output launch
+      if (cudaMallocFromPoolAsync(&tot, (size_t)BH * n_parts * (size_t)lp.tot_stride * 4u, ds->pool, s) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return FATTN_ERR_CUDA;
+      }
+      lp.tot = reinterpret_cast<float*>(tot);
+      fattn::fattn_linear_tc_kernel<true>
+          <<<(unsigned)(BH * (n_parts - 1)), fattn::LTC_THREADS, fattn::LtcCfg::SMEM_BYTES, s>>>(mq, mk, mv, lp);
+    }
+    mark_kernel_start(s);
+    fattn::fattn_linear_tc_kernel<false>
+        <<<(unsigned)(BH * n_parts), fattn::LTC_THREADS, fattn::LtcCfg::SMEM_BYTES, s>>>(mq, mk, mv, lp);
+    mark_kernel_stop(s);
+    if (cudaGetLastError() != cudaSuccess) rc = FATTN_ERR_CUDA;
+    if (tot && cudaFreeAsync(tot, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
+    return rc;
+  }
   const size_t state_floats = (size_t)BH * n_chunks * (size_t)E * M;
   const size_t ksum_floats = (size_t)BH * n_chunks * (size_t)E;
   void* scratch = nullptr;
@@ -813,24 +877,6 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   return rc;
 }
 
-extern "C" FATTN_API int fattn_last_error(void* stream, int* detail) {
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
-  DeviceState* ds = nullptr;
-  int rc = device_state(dev, &ds);
-  if (rc != FATTN_OK) return rc;
-  int h[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(h, ds->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
-  if (detail)
-    for (int i = 0; i < 4; ++i) detail[i] = h[i];
-  if (h[0] != 0) {
-    if (cudaMemset(ds->err, 0, sizeof h) != cudaSuccess) return FATTN_ERR_CUDA;
-    return FATTN_ERR_TIMEOUT;
-  }
-  return FATTN_OK;
-}
-
 // ------------------------------------------------------------------------
 // fattn_fwd_noalloc: the same forward for callers that cannot allocate
 // device memory.  Its scratch (the V copy in the P V operand type, the
@@ -950,9 +996,43 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   p.wait_limit_ns = wait_limit_ns();
   const int grid = (int)(units < ns->num_sms ? units : ns->num_sms);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the error word must start at zero for this call; the V copy and modes are fully rewritten
-  if (cudaMemsetAsync(p.err, 0, 4 * sizeof(int), s) != cudaSuccess) return FATTN_ERR_CUDA;
+  // The V copy and the tile modes are fully rewritten by this call.  The error
+  // word is zero at load and cleared by fattn_last_error when it reports a
+  // time-out, so it is not cleared here: a time-out stays readable until then.
   return d <= 64    ? enqueue<64>(q, k, v, p, ns->scratch, grid, s)
          : d <= 128 ? enqueue<128>(q, k, v, p, ns->scratch, grid, s)
                     : enqueue_d256(q, k, v, p, ns->scratch, s);
+}
+
+// ------------------------------------------------------------------------
+// fattn_last_error: the error words of both kinds of entry point on the
+// current device -- the pool-backed calls' word and the no-alloc array's --
+// read only where that kind has been set up, so it allocates nothing.
+extern "C" FATTN_API int fattn_last_error(void* stream, int* detail) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FATTN_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FATTN_ERR_CUDA;
+  int* words[2] = {nullptr, nullptr};
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_dev[dev].ready) words[0] = g_dev[dev].err;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc[dev].ready) words[1] = reinterpret_cast<int*>(g_noalloc[dev].scratch + kNoAllocScratch);
+  }
+  int first[4] = {0, 0, 0, 0};
+  for (int* word : words) {
+    if (!word) continue;
+    int h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, word, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (h[0] == 0) continue;
+    if (cudaMemset(word, 0, sizeof h) != cudaSuccess) return FATTN_ERR_CUDA;
+    if (first[0] == 0)
+      for (int i = 0; i < 4; ++i) first[i] = h[i];
+  }
+  if (detail)
+    for (int i = 0; i < 4; ++i) detail[i] = first[i];
+  return first[0] != 0 ? FATTN_ERR_TIMEOUT : FATTN_OK;
 }

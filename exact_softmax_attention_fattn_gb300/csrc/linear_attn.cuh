@@ -48,9 +48,15 @@ struct LinParams {
   float eps;
 };
 
-// elu(x) + 1; the fast exponential's error (a few ulp on x <= 0) is far below
-// the fp32 summation error of the sums it feeds
-__device__ __forceinline__ float lin_phi(float x) { return x > 0.0f ? x + 1.0f : __expf(x); }
+// elu(x) + 1, branch-free: max(x, 0) + 2^(min(x, 0) log2 e) is x + 1 for
+// x > 0 (2^0 = 1) and e^x otherwise; the fast exponential's error (a few ulp
+// on x <= 0) is far below the fp32 summation error of the sums it feeds.  (A
+// select between x + 1 and e^x compiled to a divergent branch per element.)
+__device__ __forceinline__ float lin_phi(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(x, 0.0f) * 1.4426950408889634f));
+  return fmaxf(x, 0.0f) + e;
+}
 
 __device__ __forceinline__ int lin_key_len(const LinParams& p, int bh) {
   int kl = p.key_len ? p.key_len[bh / p.H] : p.N;

@@ -320,6 +320,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// 16 registers per thread -> 16 consecutive 32-bit TMEM columns of this warp's lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -384,6 +394,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+// The two halves of a packed bf16x2 widened exactly to fp32 (a bf16 is the
+// upper 16 bits of the fp32 with the same value).
+__device__ __forceinline__ float bf16lo_as_f32(uint32_t b2) { return __uint_as_float(b2 << 16); }
+__device__ __forceinline__ float bf16hi_as_f32(uint32_t b2) { return __uint_as_float(b2 & 0xFFFF0000u); }
 
 // Packed f16x2 -> packed bf16x2 (each half widened exactly, then rounded to
 // nearest even).

@@ -219,6 +219,15 @@ def linear_flops(w: LinearWorkload) -> float:
     return float(w.B * w.H * w.N) * (4.0 * w.E * w.M + 4.0 * w.E)
 
 
+def algorithmic_bytes(w: Workload, key_len: np.ndarray | None = None) -> float:
+    """HBM bytes one forward must move at least: Q read, O written (bf16) and
+    LSE written (fp32) for every row, and the K and V rows some query can see
+    (all N under the causal mask; the first key_len[b] with key padding)."""
+    rows = float(w.B * w.H * w.N)
+    kv_rows = rows if key_len is None else float(w.H) * float(np.sum(np.clip(key_len, 0, w.N)))
+    return rows * w.d * 2 * 2 + rows * 4 + kv_rows * w.d * 2 * 2
+
+
 def causal_flops(w: Workload, key_len: np.ndarray | None = None) -> float:
     """Algorithmic FLOPs of one forward: 4*B*H*N^2*d, half of it when causal;
     with key padding, 4*H*N*d*sum(key_len)."""

@@ -37,11 +37,18 @@
 extern "C" {
 #endif
 
-/* Status codes returned by every entry point. */
+/*
+ * Status codes returned by every entry point.  Zero is success and any
+ * configuration the library does not run gets a non-zero code instead of a
+ * launch: the convention of the host dispatch of the "Linear Attention CUDA
+ * kernel" page (its `lmha` entry returns a non-zero value for a feature size
+ * it has no kernel for), with the cause split into the codes below.
+ */
 typedef enum {
   FATTN_OK = 0,
   FATTN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or scale is invalid */
-  FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration the library runs (head dim) */
+  FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration the library runs (head dim,
+                                split-KV or backward above head dim 128, no-alloc size) */
   FATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FATTN_ERR_TIMEOUT = 4      /* a bounded wait inside the kernel gave up (see fattn_last_error) */
 } fattn_status;
@@ -56,10 +63,11 @@ typedef enum {
  *   lse      device pointer, fp32, [B, H, N] contiguous, written (natural log).
  *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 0.
  *            If B*H*N == 0 the call does nothing and returns FATTN_OK.
- *   d        head dim: a multiple of 8 from 8 to 128 (others return
+ *   d        head dim: a multiple of 8 from 8 to 256 (others return
  *            FATTN_ERR_UNSUPPORTED).  d <= 64 runs in the 64-column kernel,
- *            larger d in the 128-column one; the columns past d are read as
- *            zeros and never stored, so rows stay d elements long.
+ *            72..128 in the 128-column one, 136..256 in the 256-column
+ *            kernel (one query tile per CTA, never split); the columns past d
+ *            are read as zeros and never stored, so rows stay d elements long.
  *   scale    softmax scale applied to Q K^T before the mask; finite and >= 0
  *            (usually 1/sqrt(d)).
  *   causal   nonzero: key j is visible to query i only if j <= i.
@@ -77,8 +85,8 @@ typedef enum {
  * the operand type of the P V product (fp16 per 128-row tile where V's
  * range allows, else bf16), so the probabilities P are rounded to fp16.
  *
- * Split-KV: when the problem has fewer blocks of 256 query rows than the GPU
- * has SMs, the call may split each block's key range (the split count that
+ * Split-KV (head dims up to 128): when the problem has fewer blocks of 256
+ * query rows than the GPU has SMs, the call may split each block's key range (the split count that
  * fattn_splitkv_plan(B, H, N, causal, SMs, 0) returns) and merge the
  * splits' partial results with the two-block rule ("understand-
  * flashattention", two-block online-softmax derivation); the scratch then
@@ -94,7 +102,7 @@ typedef enum {
  * Returns FATTN_OK, FATTN_ERR_INVALID_ARG (null pointer with B*H*N > 0,
  * negative size, misaligned pointer, host pointer, non-finite or negative
  * scale, sizes beyond int32 index space), FATTN_ERR_UNSUPPORTED (d not a
- * multiple of 8 in [8, 128]) or FATTN_ERR_CUDA (launch failed; no kernel ran).  Argument errors
+ * multiple of 8 in [8, 256]) or FATTN_ERR_CUDA (launch failed; no kernel ran).  Argument errors
  * are detected before anything is enqueued.
  */
 FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -116,7 +124,9 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
  *            key_len: bf16 O [B, H, N, d] and fp32 LSE [B, H, N].
  *   dout     dL/dO, bf16 [B, H, N, d].
  *   dq, dk, dv  written: bf16 [B, H, N, d]; each rounded once from fp32.
- *   B, H, N, d, scale, causal, key_len, stream: as for fattn_fwd.
+ *   B, H, N, scale, causal, key_len, stream: as for fattn_fwd.
+ *   d        head dim: a multiple of 8 from 8 to 128 (the backward has no
+ *            256-column kernel; 136..256 return FATTN_ERR_UNSUPPORTED).
  *
  * A query row with no visible key gets dQ = 0; a key visible to no query
  * (key_len) gets dK = dV = 0.  All device pointers 16-byte aligned (lse and
@@ -147,10 +157,13 @@ FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void*
  *             combine kernel:
  *                 LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
  *             over the splits that hold keys of the row.
- *             Negative: FATTN_ERR_INVALID_ARG.
+ *             Negative: FATTN_ERR_INVALID_ARG.  Above head dim 128 only 0
+ *             and 1 are accepted (the 256-column kernel never splits); k > 1
+ *             there returns FATTN_ERR_UNSUPPORTED before anything is enqueued.
  *
  * Every other argument, the layouts, ownership and errors are those of
- * fattn_fwd; the scratch is as described there for the split count used.
+ * fattn_fwd (head dims: multiples of 8 from 8 to 256); the scratch is as
+ * described there for the split count used.
  */
 FATTN_API int fattn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                 int N, int d, float scale, int causal, const int32_t* key_len, int n_splits,
@@ -165,7 +178,8 @@ FATTN_API int fattn_fwd_splitkv(const void* q, const void* k, const void* v, voi
  *            block the calling thread).
  *   o, lse   host pointers, written: bf16 O [B, H, N, d] and fp32 LSE [B, H, N].
  *   key_len  host pointer to int32[B] or NULL.
- *   Other arguments as for fattn_fwd; head dims as for fattn_fwd.
+ *   Other arguments as for fattn_fwd; head dims as for fattn_fwd
+ *   (multiples of 8 from 8 to 256).
  *
  * The call takes device buffers for Q, K, V, O, LSE and key_len from the
  * library's pool, cuts the problem into up to eight chunks (ranges of whole
@@ -243,16 +257,25 @@ FATTN_API int fattn_linear_fwd(const float* q, const float* k, const float* v, f
  */
 FATTN_API int fattn_set_kernel_events(void* start, void* stop);
 
-/* A static, human-readable name for a status code. */
+/*
+ * A static, human-readable name for a status code (the non-zero codes of the
+ * return-code convention described at fattn_status); never NULL: an unknown
+ * code gives "unknown status".
+ */
 FATTN_API const char* fattn_status_string(int status);
 
 /*
  * Synchronises `stream` and reports whether any fattn kernel on the current
  * device timed out in a bounded wait since the last call: FATTN_ERR_TIMEOUT
  * (and clears the flag), FATTN_ERR_CUDA if the synchronisation failed, else
- * FATTN_OK.  If detail is not NULL it receives 4 ints: status, role
- * (1 softmax, 2 TMA producer, 3 MMA issuer), barrier id and work unit of the
- * first time-out.
+ * FATTN_OK -- a device-side failure reported as a non-zero code, the same
+ * convention as the entry points' own returns (see fattn_status).  It reads
+ * the error word of the pool-backed entry points and the one inside the
+ * no-alloc array (fattn_fwd_noalloc), each only once that kind of call has
+ * set itself up on this device, so it allocates nothing itself.  If detail
+ * is not NULL it receives 4 ints: status, role (1 softmax, 2 TMA producer,
+ * 3 MMA issuer), barrier id and work unit of the first time-out (the
+ * pool-backed word's when both hold one), or zeros.
  */
 FATTN_API int fattn_last_error(void* stream, int* detail);
 
@@ -281,18 +304,19 @@ FATTN_API int fattn_last_error(void* stream, int* detail);
  *       round_up(B*H*N*d*2, 256) + round_up(B*H*round_up(ceil(N/128), 8), 256)
  *         <= 64 MiB
  *     (for example B*H <= 63 at N = 4096, d = 128); larger problems return
- *     FATTN_ERR_UNSUPPORTED before anything is enqueued.
+ *     FATTN_ERR_UNSUPPORTED before anything is enqueued.  Head dims as for
+ *     fattn_fwd: multiples of 8 from 8 to 256.
  *   - Set-up: the first call on a device (with that device current) looks up
  *     the array's device address and sets kernel attributes; make that first
  *     call before any stream capture.
  *   - Sharing: every call uses the same array and it keeps the last call's
- *     contents.  Each call clears the error word (an async memset on
- *     `stream`) and rewrites the V copy it reads, so nothing carries over
- *     from one call to the next; but calls whose kernels overlap on the GPU
- *     (different streams with no ordering between them) race on the array
- *     and give wrong results.
- *   - Time-outs of the kernel's bounded waits land in the array's error word;
- *     fattn_last_error() does not read it.
+ *     contents.  Each call rewrites the V copy and tile modes it reads, so no
+ *     data carries over from one call to the next; but calls whose kernels
+ *     overlap on the GPU (different streams with no ordering between them)
+ *     race on the array and give wrong results.
+ *   - Time-outs of the kernel's bounded waits land in an error word after
+ *     the array (zero at load).  fattn_last_error() reads and clears it, so
+ *     a time-out stays readable until then, even across later calls.
  */
 FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                 int N, int d, float scale, int causal, const int32_t* key_len, void* stream);

@@ -241,3 +241,71 @@ def test_noalloc_validates_like_fattn_fwd(lib):
     assert na(q=FAKE + 8) == binding.FATTN_ERR_INVALID_ARG  # not 16-byte aligned
     # beyond the static scratch: B*H*N*d*2 bytes of V copy alone exceed 64 MiB
     assert na(B=64, H=16, N=4096, d=128) == binding.FATTN_ERR_UNSUPPORTED
+
+
+def _decl_comment(name: str) -> str:
+    """The comment block directly above an entry point's declaration in include/fattn.h."""
+    text = open(os.path.join(ROOT, "include", "fattn.h")).read()
+    i = re.search(r"FATTN_API[^;(]*\b" + name + r"\(", text).start()
+    j = text.rindex("/*", 0, i)
+    return "\n".join(re.sub(r"^\s*\*+/?\s?", "", ln) for ln in text[j:i].splitlines())
+
+
+def _stated_max_head_dim(name: str, split: bool = False) -> int:
+    """The largest head dim the header states for an entry point ('a multiple
+    of 8 from 8 to D'); for fattn_fwd_splitkv with split=True, the bound it
+    states for k > 1 splits ('Above head dim D only 0 and 1')."""
+    c = " ".join(_decl_comment(name).split())
+    if split:
+        return int(re.search(r"Above head dim (\d+) only 0 and 1", c).group(1))
+    m = re.search(r"multiples? of 8 from 8 to (\d+)", c)
+    assert m, f"{name}: the header states no head-dim range"
+    return int(m.group(1))
+
+
+def _first_refused(call_d) -> int:
+    """Largest d in 8, 16, ... that the entry point accepts (its status is not
+    FATTN_ERR_UNSUPPORTED with fake host pointers, which fail later checks)."""
+    best = 0
+    for d in range(8, 513, 8):
+        if call_d(d) != binding.FATTN_ERR_UNSUPPORTED:
+            assert best == d - 8, f"accepted head dims are not contiguous at {d}"
+            best = d
+    return best
+
+
+def test_header_head_dim_ranges_match_the_library(lib):
+    """Each entry point's stated head-dim range is exactly what it accepts:
+    every multiple of 8 up to the stated maximum passes the head-dim check,
+    the next one is refused with FATTN_ERR_UNSUPPORTED, and no other d passes."""
+    fwd = lambda d: call(d=d)
+    host = lambda d: hcall(d=d)
+    bwd = lambda d: bcall(d=d)
+    noalloc = lambda d: binding.noalloc_raw(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, d, 0.125, False, None, None)
+
+    def splitk(n):
+        return lambda d: binding.fwd_raw(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, d, 0.125, 0, None, None, n)
+
+    cases = [("fattn_fwd", fwd, False), ("fattn_fwd_host", host, False), ("fattn_fwd_noalloc", noalloc, False),
+             ("fattn_bwd", bwd, False), ("fattn_fwd_splitkv", splitk(0), False),
+             ("fattn_fwd_splitkv", splitk(1), False), ("fattn_fwd_splitkv", splitk(2), True)]
+    for name, fn, split in cases:
+        stated = _stated_max_head_dim(name, split)
+        assert _first_refused(fn) == stated, (name, split, stated)
+        for d in (4, 12, stated + 4, stated + 8):
+            assert fn(d) == binding.FATTN_ERR_UNSUPPORTED, (name, d)
+    # the forward's own statement of its range
+    assert _stated_max_head_dim("fattn_fwd") == 256
+    assert _stated_max_head_dim("fattn_bwd") == 128
+
+
+def test_status_codes_cite_their_convention():
+    """The status enum, fattn_status_string and fattn_last_error cite the
+    pages' non-zero-return convention."""
+    text = open(os.path.join(ROOT, "include", "fattn.h")).read()
+    enum_comment = text[text.rindex("/*", 0, text.index("typedef enum")):text.index("typedef enum")]
+    enum_comment = " ".join(re.sub(r"^\s*\*+/?\s?", "", ln) for ln in enum_comment.splitlines()).split()
+    enum_comment = " ".join(enum_comment)
+    assert "Linear Attention CUDA kernel" in enum_comment and "lmha" in enum_comment
+    for name in ("fattn_status_string", "fattn_last_error"):
+        assert "convention" in _decl_comment(name), name

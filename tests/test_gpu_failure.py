@@ -30,7 +30,7 @@ from exact_softmax_attention_fattn_gb300.inputs import Workload, make_inputs
 # shapes whose waits run well past 1 us: the 256-column kernel, whose CTAs
 # each hold one query tile, gets a non-causal problem (every CTA 64 key tiles)
 shapes = {"fwd": (1, 4, 2048, 128, True), "split": (1, 2, 4096, 128, True), "d256": (1, 8, 4096, 256, False),
-          "bwd": (1, 2, 1024, 128, True)}
+          "bwd": (1, 2, 1024, 128, True), "noalloc": (1, 4, 2048, 128, True), "linear": (2, 4, 4096, 64, True)}
 B, H, N, d, causal = shapes[case]
 x = make_inputs(Workload("to", B, H, N, d, causal, 50))
 dev = torch.device("cuda:0")
@@ -40,6 +40,16 @@ if case == "bwd":
     binding.last_error()                  # start clean
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     binding.backward_into(q, k, v, o, lse, q, dq, dk, dv, causal=causal)
+elif case == "linear":
+    # causal linear attention on the tensor cores (fp32 Q, K, V; E = M = 64)
+    lq, lk, lv = (torch.randn(B, H, N, d, device=dev) for _ in range(3))
+    binding.linear_forward(lq, lk, lv)
+elif case == "noalloc":
+    # the no-alloc entry point records its time-out in the word after its
+    # static array; fattn_last_error must report it like the others
+    st0 = binding.noalloc_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                              1.0 / d ** 0.5, int(causal), None, torch.cuda.current_stream().cuda_stream)
+    assert st0 == 0, st0
 else:
     binding.forward_into(q, k, v, o, lse, causal=causal, n_splits=4 if case == "split" else None)
 st, detail = binding.last_error()
@@ -51,11 +61,12 @@ print(json.dumps({"status": st, "detail": detail, "again": again, "context_ok": 
 """
 
 
-@pytest.mark.parametrize("case", ["fwd", "split", "d256", "bwd"])
+@pytest.mark.parametrize("case", ["fwd", "split", "d256", "bwd", "noalloc", "linear"])
 def test_bounded_wait_times_out_and_reports(cuda_device, case):
     """Each kernel family (the forward, its split-KV instantiation, the
-    256-column forward, the backward's kernels) times out for real and
-    reports; the backward runs on zero O and LSE (values do not matter
+    256-column forward, the backward's kernels, the tensor-core linear
+    attention kernels) and the no-alloc entry point (its error word lives
+    after its static array) times out for real and reports; the backward runs on zero O and LSE (values do not matter
     here)."""
     env = dict(os.environ, FATTN_WAIT_LIMIT_US="1")
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT, case], env=env, capture_output=True, text=True,
