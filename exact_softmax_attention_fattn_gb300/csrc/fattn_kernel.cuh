@@ -38,7 +38,10 @@
 //     than 2^8 since the last rescale: O and l keep a common, slightly stale
 //     reference, so the final O / l is unchanged (exact up to rounding).
 //   * every wait is bounded; on time-out the kernel records an error word,
-//     drains its own copies and MMAs, frees tensor memory and returns.
+//     drains its own copies and MMAs, frees tensor memory and returns;
+//   * when launched as a programmatic dependent of the V pre-pass (small
+//     grids), the producer loads Q and K before griddepcontrol.wait and V
+//     after it, and the other roles wait before reading the V tile modes.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -239,6 +242,7 @@ __device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r
 // global load at a unit boundary, where the epilogue's output stores occupy
 // the memory pipeline.
 struct UnitIter {
+  bool modes = true;       // read the V storage modes (not in the producer)
   int r, u, kl_raw;        // current unit (u < 0: done)
   int mode0;               // storage mode of its first V tile
   int r_next, u_next;      // the one after it
@@ -254,7 +258,7 @@ struct UnitIter {
   __device__ __forceinline__ void load_next(const Params& p) {
     if (u_next < 0) return;
     kl_next = p.key_len ? __ldg(p.key_len + next_bh / p.H) : p.N;
-    mode_next = __ldg(p.v_mode + (size_t)next_bh * p.mode_stride);  // (split units read theirs at the unit start)
+    if (modes) mode_next = __ldg(p.v_mode + (size_t)next_bh * p.mode_stride);  // (split units read theirs at the unit start)
   }
   __device__ __forceinline__ void locate_next(const Params& p, int cta, int G) {
     r_next = r < 0 ? -1 : round_from(p, r + 1, cta, G);
@@ -268,7 +272,7 @@ struct UnitIter {
     if (u >= 0) {
       const int bh = u % (p.B * p.H);
       kl_raw = p.key_len ? __ldg(p.key_len + bh / p.H) : p.N;
-      mode0 = __ldg(p.v_mode + (size_t)bh * p.mode_stride);
+      if (modes) mode0 = __ldg(p.v_mode + (size_t)bh * p.mode_stride);
     }
     locate_next(p, cta, G);
     load_next(p);
@@ -452,6 +456,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++g;
       };
       UnitIter it;
+      it.modes = false;
+      bool v_ready = false;  // the V copy (the pre-pass's output) waited for
       it.begin(p, cta, G);
       for (; ok && it.u >= 0; it.advance(p, cta, G)) {
         const int u = it.u;
@@ -471,6 +477,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t bit = 1u << (gk % 32u);
           two = ntiles == 2u ? (two | bit) : (two & ~bit);
           ++gk;
+          if (has_v && !v_ready) {
+            pdl_wait();
+            v_ready = true;
+          }
           if (has_v) load_kv(&tmap_v, w.j0 + j, w.bh, full);
           if (has_k) {
             make_room(g, gk - 1u, u);
@@ -542,6 +552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         });
       };
 
+      pdl_wait();  // the V storage modes come from the pre-pass
       UnitIter it;
       it.begin(p, cta, G);
       for (; ok && it.u >= 0; it.advance(p, cta, G)) {
@@ -646,6 +657,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
 
+    pdl_wait();  // the V storage modes come from the pre-pass
     UnitIter it;
     it.begin(p, cta, G);
     for (; ok && it.u >= 0; it.advance(p, cta, G)) {

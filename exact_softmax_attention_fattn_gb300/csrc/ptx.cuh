@@ -346,6 +346,15 @@ __device__ __forceinline__ void regs_shrink() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel launched as a programmatic dependent of the previous one in its
+// stream may start before that one ends: the previous kernel lets it launch
+// (launch_dependents), and it waits (wait) for the previous kernel's
+// completion and memory before reading what that kernel wrote.  Both are
+// no-ops outside such a launch.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- math
 // Packed pairs of fp32 (sm_100+ f32x2 arithmetic: one instruction, two lanes of work).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {

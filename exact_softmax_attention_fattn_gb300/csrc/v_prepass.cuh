@@ -30,6 +30,7 @@ template <int D, bool FULL>
 __global__ void __launch_bounds__(prepass_threads<D>())
     fattn_v_prepass_kernel(const uint4* __restrict__ v, uint4* __restrict__ v16, uint8_t* __restrict__ mode, int N,
                            int hd_arg, int n_tiles, int mode_stride) {
+  pdl_launch_dependents();  // the attention kernel may start its set-up now (it waits before reading V)
   const int hd = FULL ? D : hd_arg;
   constexpr int VEC = 8;                                  // bf16 per 16-byte vector
   constexpr int T = prepass_threads<D>();
