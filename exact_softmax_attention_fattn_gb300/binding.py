@@ -24,7 +24,7 @@ FATTN_ERR_TIMEOUT = 4
 
 EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_fwd_noalloc", "fattn_splitkv_plan",
             "fattn_bwd", "fattn_linear_fwd", "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error",
-            "fattn_version")
+            "fattn_version", "fattn_tensor_map_stats")
 
 _lock = threading.Lock()
 _lib = None
@@ -89,6 +89,8 @@ def load_library():
             lib.fattn_last_error.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
             lib.fattn_version.restype = ctypes.c_int
             lib.fattn_version.argtypes = []
+            lib.fattn_tensor_map_stats.restype = ctypes.c_int
+            lib.fattn_tensor_map_stats.argtypes = [ctypes.POINTER(ctypes.c_longlong)] * 2
             _lib = lib
     return _lib
 
@@ -181,6 +183,13 @@ def bwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, do_ptr: int, lse_ptr
     """fattn_bwd with raw addresses; returns the status code."""
     return load_library().fattn_bwd(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, int(B),
                                     int(H), int(N), int(d), float(scale), int(bool(causal)), key_len_ptr, stream)
+
+
+def tensor_map_stats() -> tuple[int, int]:
+    """fattn_tensor_map_stats: (reused, freshly encoded) tensor maps since load."""
+    hits, misses = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    load_library().fattn_tensor_map_stats(ctypes.byref(hits), ctypes.byref(misses))
+    return hits.value, misses.value
 
 
 def last_error(stream=None) -> tuple[int, list[int]]:

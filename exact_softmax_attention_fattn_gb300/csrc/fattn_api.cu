@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -200,12 +201,61 @@ bool is_device_pointer(const void* ptr) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// Tensor maps already encoded, keyed by everything a map is made from
+// (address, shape, element type, box): a map depends on nothing else, so a
+// hit is exactly the map that encoding again would give, even when the
+// memory behind the address was freed and reallocated meanwhile.  Encoding
+// is host work repeated on every call of a training or serving loop, where
+// the same buffers come back call after call.
+struct MapKey {
+  const void* ptr;
+  int BH, N, d;
+  int type;
+  unsigned box_rows;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && BH == o.BH && N == o.N && d == o.d && type == o.type && box_rows == o.box_rows;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_maps_used = 0, g_maps_next = 0;
+std::atomic<long long> g_map_hits{0}, g_map_misses{0};
+
+bool map_lookup(const MapKey& key, CUtensorMap* map) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < g_maps_used; ++i)
+    if (g_maps[i].key == key) {
+      *map = g_maps[i].map;
+      return true;
+    }
+  return false;
+}
+
+void map_insert(const MapKey& key, const CUtensorMap& map) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < g_maps_used; ++i)
+    if (g_maps[i].key == key) return;  // another thread got there first
+  g_maps[g_maps_next] = MapEntry{key, map};
+  g_maps_next = (g_maps_next + 1) % kMapCache;
+  if (g_maps_used < kMapCache) ++g_maps_used;
+}
+
 // [B*H, N, d] 16-bit elements viewed as a 3-D tensor: x = head dim (innermost),
 // y = row, z = batch*head.  Boxes of 64 x box_rows x 1 with 128-byte swizzle;
 // rows past N and columns past d (head dims below the kernel's column count)
 // read as zero.
 int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensorMapDataType type,
                unsigned box_rows = 128u) {
+  const MapKey key{ptr, BH, N, d, (int)type, box_rows};
+  if (map_lookup(key, map)) {
+    g_map_hits.fetch_add(1, std::memory_order_relaxed);
+    return FATTN_OK;
+  }
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2ull, (cuuint64_t)N * (cuuint64_t)d * 2ull};
   cuuint32_t box[3] = {64u, box_rows, 1u};
@@ -213,7 +263,10 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
   CUresult r = g_encode(map, type, 3, const_cast<void*>(ptr), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return FATTN_ERR_CUDA;
+  g_map_misses.fetch_add(1, std::memory_order_relaxed);
+  map_insert(key, *map);
+  return FATTN_OK;
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -222,6 +275,11 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // without swizzle (rows of 256 bytes in shared memory); columns past F and
 // rows past N read as zero.
 int encode_map_f32(CUtensorMap* map, const void* ptr, int BH, int N, int F) {
+  const MapKey key{ptr, BH, N, F, (int)CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (unsigned)fattn::LTC_T};
+  if (map_lookup(key, map)) {
+    g_map_hits.fetch_add(1, std::memory_order_relaxed);
+    return FATTN_OK;
+  }
   cuuint64_t dims[3] = {(cuuint64_t)F, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)F * 4ull, (cuuint64_t)N * (cuuint64_t)F * 4ull};
   cuuint32_t box[3] = {(cuuint32_t)fattn::LTC_F, (cuuint32_t)fattn::LTC_T, 1u};
@@ -229,7 +287,10 @@ int encode_map_f32(CUtensorMap* map, const void* ptr, int BH, int N, int F) {
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, elem,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FATTN_OK : FATTN_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return FATTN_ERR_CUDA;
+  g_map_misses.fetch_add(1, std::memory_order_relaxed);
+  map_insert(key, *map);
+  return FATTN_OK;
 }
 
 // Head dims the kernels run: multiples of 8 (rows of 16-byte vectors, TMA
@@ -450,6 +511,12 @@ bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 }  // namespace
 
 extern "C" FATTN_API int fattn_version(void) { return 100; }
+
+extern "C" FATTN_API int fattn_tensor_map_stats(long long* hits, long long* misses) {
+  if (hits) *hits = g_map_hits.load(std::memory_order_relaxed);
+  if (misses) *misses = g_map_misses.load(std::memory_order_relaxed);
+  return FATTN_OK;
+}
 
 extern "C" FATTN_API const char* fattn_status_string(int status) {
   switch (status) {

@@ -406,20 +406,29 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld64(s_addr, sh);
           tmem_ld_wait(sh);
           uint32_t pk[32];
+          // a separate copy of the loop for tiles with masked columns, so
+          // that the others carry no per-element selects
+          auto p_loop = [&](auto masked_c) {
+            constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4) {
-            const float4 l4 = lse4[q4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            for (int q4 = 0; q4 < 16; ++q4) {
+              const float4 l4 = lse4[q4];
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = 64 * g + 4 * q4 + e;
-              float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
-              if (any_mask) pe = (key_vis && col >= min_q) ? pe : 0.0f;
-              pr[4 * q4 + e] = pe;
+              for (int e = 0; e < 4; ++e) {
+                const int col = 64 * g + 4 * q4 + e;
+                float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
+                if constexpr (MASKED) pe = (key_vis && col >= min_q) ? pe : 0.0f;
+                pr[4 * q4 + e] = pe;
+              }
+              pk[2 * q4] = pack_bf16x2(pr[4 * q4], pr[4 * q4 + 1]);
+              pk[2 * q4 + 1] = pack_bf16x2(pr[4 * q4 + 2], pr[4 * q4 + 3]);
             }
-            pk[2 * q4] = pack_bf16x2(pr[4 * q4], pr[4 * q4 + 1]);
-            pk[2 * q4 + 1] = pack_bf16x2(pr[4 * q4 + 2], pr[4 * q4 + 3]);
-          }
+          };
+          if (any_mask)
+            p_loop(std::true_type{});
+          else
+            p_loop(std::false_type{});
           tmem_st32(s_addr, pk);
         }
         tmem_st_wait();
@@ -705,12 +714,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           uint32_t sh[64];
           tmem_ld64(s_addr, sh);
           tmem_ld_wait(sh);
+          // a separate copy of the loop for masked tiles (no per-element
+          // selects on the others)
+          auto p_loop = [&](auto masked_c) {
+            constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
-          for (int q = 0; q < 64; ++q) {
-            float pe = ex2(fmaf(__uint_as_float(sh[q]), c, -lse2));
-            if (masked) pe = q < vis_n ? pe : 0.0f;
-            pr[q] = pe;
-          }
+            for (int q = 0; q < 64; ++q) {
+              float pe = ex2(fmaf(__uint_as_float(sh[q]), c, -lse2));
+              if constexpr (MASKED) pe = q < vis_n ? pe : 0.0f;
+              pr[q] = pe;
+            }
+          };
+          if (masked)
+            p_loop(std::true_type{});
+          else
+            p_loop(std::false_type{});
         }
         // phase 2: dS = P (dP - D), stored as bf16 over this group's first 32 columns of S
         ok = wait_bar(waiter, bar(C::B_DP_FULL), n & 1, C::B_DP_FULL, u);

@@ -326,18 +326,34 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
         const uint64_t nmc2 = f2_pack(-mc, -mc);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[32];
-        const bool f16 = vmode == VMODE_F16;
+        // one copy of the loop per (mask, operand type), so that the common
+        // case (no mask, fp16) carries no per-element selects
+        auto exp_loop = [&](auto masked_c, auto f16_c) {
+          constexpr bool MASKED = decltype(masked_c)::value, F16 = decltype(f16_c)::value;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(sr[2 * q], sr[2 * q + 1]), c2, nmc2), x0, x1);
-          float p0 = ex2(x0), p1 = ex2(x1);
-          if (masked_tile) {
-            p0 = 2 * q < vis_n ? p0 : 0.0f;
-            p1 = 2 * q + 1 < vis_n ? p1 : 0.0f;
+          for (int q = 0; q < 32; ++q) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(sr[2 * q], sr[2 * q + 1]), c2, nmc2), x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if constexpr (MASKED) {
+              p0 = 2 * q < vis_n ? p0 : 0.0f;
+              p1 = 2 * q + 1 < vis_n ? p1 : 0.0f;
+            }
+            acc[q % 4] = f2_add(acc[q % 4], f2_pack(p0, p1));
+            pk[q] = F16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
-          acc[q % 4] = f2_add(acc[q % 4], f2_pack(p0, p1));
-          pk[q] = f16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        };
+        const bool f16 = vmode == VMODE_F16;
+        if (masked_tile) {
+          if (f16)
+            exp_loop(std::true_type{}, std::true_type{});
+          else
+            exp_loop(std::true_type{}, std::false_type{});
+        } else {
+          if (f16)
+            exp_loop(std::false_type{}, std::true_type{});
+          else
+            exp_loop(std::false_type{}, std::false_type{});
         }
         float a0, a1, a2, a3, a4, a5, a6, a7;
         f2_unpack(acc[0], a0, a1);

@@ -524,32 +524,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t ring_kdesc0 = smem_desc(base + C::RING_OFF, 16, 1024);
       const uint64_t ring_vdesc0 = smem_desc(base + C::RING_OFF, PANEL_BYTES, 1024);
 
-      // S_t = Q_t K^T from the K tile in `slot`.
+      // S_t = Q_t K^T from the K tile in `slot` (D/16 MMAs behind one elect).
       auto issue_s = [&](auto tc, uint32_t slot) {
         constexpr int t = decltype(tc)::value;
         const uint64_t qd = q_desc0 + (uint64_t)((t * C::TILE_BYTES) >> 4);
         const uint64_t kd = ring_kdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
         const uint32_t dt = tmem + TMEM_S0 + 128u * t;
-        static_for<D / 16>([&](auto kc) {
-          constexpr int kk = decltype(kc)::value;
-          constexpr uint32_t off = ((kk / 4) * PANEL_BYTES + (kk % 4) * 32u) >> 4;
-          mma_ss_w_off<off>(dt, qd, kd, IDESC_S, kk > 0 ? 1u : 0u);
-        });
+        mma_ss_batch<D / 16>(dt, qd, kd, IDESC_S, 0u);
       };
-      // P in tensor memory, V (keys x D, D contiguous) in `slot`.
-      // O_t (+)= P_t V over keys [16*KB, 16*KE) of the tile.
-      auto issue_pv = [&](auto tc, auto kb, auto ke, uint32_t slot, uint32_t accumulate, uint32_t idesc_pv) {
+      // O_t (+)= P_t V over the tile's 128 keys: P in tensor memory, V (keys x
+      // D, D contiguous) in `slot`; eight MMAs behind one elect.
+      static_assert(BN == 128, "the P V batch issues 8 MMAs of 16 keys");
+      auto issue_pv = [&](auto tc, uint32_t slot, uint32_t accumulate, uint32_t idesc_pv) {
         constexpr int t = decltype(tc)::value;
-        constexpr int KB = decltype(kb)::value, KE = decltype(ke)::value;
         const uint64_t vd = ring_vdesc0 + (uint64_t)((slot * C::TILE_BYTES) >> 4);
-        const uint32_t dt = tmem + TMEM_O0 + 128u * t;
-        const uint32_t at = tmem + TMEM_S0 + 128u * t;
-        static_for<KE - KB>([&](auto kc) {
-          constexpr int kk = KB + decltype(kc)::value;
-          constexpr uint32_t boff = (kk * 2048u) >> 4;  // 16 keys = two 1024-byte row groups
-          constexpr uint32_t acol = 8u * kk;            // 16 keys of P = 8 TMEM columns
-          mma_ts_w_off<boff, acol>(dt, at, vd, idesc_pv, kk > 0 ? 1u : accumulate);
-        });
+        mma_ts_batch8(tmem + TMEM_O0 + 128u * t, tmem + TMEM_S0 + 128u * t, vd, idesc_pv, accumulate);
       };
 
       pdl_wait();  // the V storage modes come from the pre-pass
@@ -615,7 +604,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) return;
             ++pv_cnt[t];
             tc_fence_after();
-            issue_pv(tc, TileC<0>{}, TileC<BN / 16>{}, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
+            issue_pv(tc, vslot(j), j > 0 ? 1u : 0u, idesc_pv);
             if (j == w.n(t) - 1) mma_commit_w(bar(C::B_O_FULL + t));
             if (j + 1 < w.n(t)) {
               issue_s(tc, kslot(j + 1));
@@ -783,7 +772,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nmc2 = f2_pack(-mc, -mc);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        auto half_row = [&](int h, auto pack) {
+        // MASKED: the limit tile of the row (keys at or past vis_n are zero);
+        // a separate copy of the loop, so that tiles without a mask carry no
+        // per-element selects
+        auto half_row = [&](int h, auto masked_c) {
+          constexpr bool MASKED = decltype(masked_c)::value;
           // S of this half row again (cheap to reload; keeps registers free)
           uint32_t sh[64];
           tmem_ld64(s_addr + 64u * h, sh);
@@ -796,20 +789,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[2 * q]), __uint_as_float(sh[2 * q + 1])), c2, nmc2), x0, x1);
             p0 = ex2(x0);
             p1 = ex2(x1);
-            if (masked_tile) {
+            if constexpr (MASKED) {
               p0 = i < vis_n ? p0 : 0.0f;
               p1 = i + 1 < vis_n ? p1 : 0.0f;
             }
             acc[q % 4] = f2_add(acc[q % 4], f2_pack(p0, p1));
-            pk[q] = pack(p0, p1);
+            pk[q] = pack_f16x2(p0, p1);
           }
           tmem_st32(s_addr + 32u * h, pk);
         };
-        auto both_halves = [&](auto pack) {
-          half_row(0, pack);
-          half_row(1, pack);
-        };
-        both_halves([](float a, float b) { return pack_f16x2(a, b); });
+        if (masked_tile) {
+          half_row(0, std::true_type{});
+          half_row(1, std::true_type{});
+        } else {
+          half_row(0, std::false_type{});
+          half_row(1, std::false_type{});
+        }
         if (vmode != VMODE_F16) {
           tmem_st_wait();  // the fp16 P must be in tensor memory before it is read back
 #pragma unroll 1

@@ -190,6 +190,90 @@ __device__ __forceinline__ void mma_ss_w_off2(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// N SS MMAs over K = 16*N with one elect: both descriptors advanced along K
+// (128-byte swizzled panels of 64 columns) in their low word only.
+template <int N>
+__device__ __forceinline__ void mma_ss_batch(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate);
+template <>
+__device__ __forceinline__ void mma_ss_batch<4>(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 alo, ahi, blo, bhi, al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 {alo, ahi}, %1;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.u32 al, alo, 2;\n\tadd.u32 bl, blo, 2;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 4;\n\tadd.u32 bl, blo, 4;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 6;\n\tadd.u32 bl, blo, 6;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void mma_ss_batch<8>(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 alo, ahi, blo, bhi, al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 {alo, ahi}, %1;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.u32 al, alo, 2;\n\tadd.u32 bl, blo, 2;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 4;\n\tadd.u32 bl, blo, 4;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 6;\n\tadd.u32 bl, blo, 6;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1024;\n\tadd.u32 bl, blo, 1024;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1026;\n\tadd.u32 bl, blo, 1026;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1028;\n\tadd.u32 bl, blo, 1028;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1030;\n\tadd.u32 bl, blo, 1030;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// O (+)= P V over 16*8 keys: P from tensor memory (16 keys = 8 columns), V MN-major.
+__device__ __forceinline__ void mma_ts_batch8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 blo, bhi, bl, at;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 bl, blo, 128;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 256;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 16;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 384;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 24;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 512;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 32;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 640;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 40;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 768;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 48;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 896;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 56;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // TS form with the B descriptor advanced by OFF and the A TMEM column by ACOL.
 template <uint32_t OFF, uint32_t ACOL>
 __device__ __forceinline__ void mma_ts_w_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,

@@ -321,6 +321,17 @@ FATTN_API int fattn_last_error(void* stream, int* detail);
 FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                 int N, int d, float scale, int causal, const int32_t* key_len, void* stream);
 
+/*
+ * Tensor-map cache counters (a diagnostic).  Each call describes its Q, K and
+ * V tiles to the GPU's tensor-memory-access (TMA) unit with tensor maps.  The
+ * library keeps the last 64 maps it encoded, keyed by everything a map is
+ * made from (address, shape, element type, box), and reuses one on an exact
+ * key match, so a loop that passes the same buffers encodes nothing after its
+ * first call.  Writes the number of reuses and of fresh encodings since the
+ * library was loaded (either pointer may be NULL).  Always returns FATTN_OK.
+ */
+FATTN_API int fattn_tensor_map_stats(long long* hits, long long* misses);
+
 /* Library version, major*10000 + minor*100 + patch. */
 FATTN_API int fattn_version(void);
 
