@@ -88,8 +88,10 @@ int configure_fwd_kernel() {
 
 template <bool FULL>
 int configure_d256_kernel() {
-  return cudaFuncSetAttribute(fattn::fattn_fwd_d256_kernel<FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)fattn::D256Cfg::SMEM_BYTES) == cudaSuccess
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  const int bytes = (int)fattn::D256Cfg::SMEM_BYTES;
+  return cudaFuncSetAttribute(fattn::fattn_fwd_d256_kernel<FULL, false>, attr, bytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_fwd_d256_kernel<FULL, true>, attr, bytes) == cudaSuccess
              ? FATTN_OK
              : FATTN_ERR_CUDA;
 }
@@ -390,6 +392,18 @@ int plan_splits(int B, int H, int N, int causal, int num_sms, int requested) {
   return best;
 }
 
+// K/V splits per query tile of the head-dim-256 kernel (one CTA per 128-row
+// query tile and split, 64-key tiles).  requested > 0: that many, at most one
+// per key tile; 0: when the query tiles alone leave SMs idle, enough splits
+// to give every SM a CTA, keeping at least two key tiles per split.
+int plan_splits_d256(int B, int H, int N, int num_sms, int requested) {
+  const long long n_kv = (N + fattn::D256_BN - 1) / fattn::D256_BN;
+  const long long tiles = (long long)B * H * ((N + fattn::BM - 1) / fattn::BM);
+  if (requested > 0) return (int)std::min<long long>(requested, std::max<long long>(1, n_kv));
+  if (tiles >= num_sms || n_kv < 4) return 1;
+  return (int)std::max<long long>(1, std::min<long long>({num_sms / tiles, n_kv / 2, (long long)kMaxSplits}));
+}
+
 // Enqueues the V pre-pass, the attention kernel and, with split-KV, the
 // combine kernel; `scratch` must hold scratch_bytes(..., p.n_splits).
 template <int D>
@@ -461,19 +475,27 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
     constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 16);
     const dim3 cgrid((unsigned)((p.N + rows_per_block - 1) / rows_per_block), (unsigned)(BH < 65535 ? BH : 65535));
     fattn::fattn_splitkv_combine_kernel<D><<<cgrid, fattn::COMBINE_THREADS, 0, stream>>>(
-        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.hd, p.causal, p.n_splits);
+        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.hd, p.causal, p.n_splits,
+        fattn::QT * fattn::BM, fattn::BN);
     if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   }
   return FATTN_OK;
 }
 
-// Head dims 136..256: V pre-pass and the one-query-tile kernel (no split-KV);
-// `scratch` must hold scratch_bytes(..., 1).
+// Head dims 136..256: V pre-pass, the one-query-tile kernel and, with
+// split-KV (p.n_splits > 1), the combine kernel; `scratch` must hold
+// scratch_bytes(..., p.n_splits).
 int enqueue_d256(const void* q, const void* k, const void* v, fattn::Params p, void* scratch, cudaStream_t stream) {
   const int BH = p.B * p.H;
   uint8_t* v16 = reinterpret_cast<uint8_t*>(scratch);
   uint8_t* modes = v16 + round_up((size_t)BH * (size_t)p.N * (size_t)p.hd * 2u, 256);
   p.v_mode = modes;
+  if (p.n_splits > 1) {
+    uint8_t* part = modes + round_up((size_t)BH * round_up((size_t)p.n_kv_tiles, 8), 256);
+    p.o_part = reinterpret_cast<float*>(part);
+    p.lse_part =
+        reinterpret_cast<float*>(part + round_up((size_t)p.n_splits * BH * (size_t)p.N * (size_t)p.hd * 4u, 256));
+  }
   CUtensorMap mq, mk, mv;
   if (encode_map(&mq, q, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128u) != FATTN_OK ||
       encode_map(&mk, k, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (unsigned)fattn::D256_BN) != FATTN_OK ||
@@ -490,20 +512,34 @@ int enqueue_d256(const void* q, const void* k, const void* v, fattn::Params p, v
         reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(v16), modes, p.N, p.hd, p.n_kv_tiles,
         p.mode_stride);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  const long long ctas = (long long)BH * ((p.N + fattn::BM - 1) / fattn::BM);
+  const long long ctas = (long long)BH * ((p.N + fattn::BM - 1) / fattn::BM) * p.n_splits;
   if (ctas > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   // heads per group of the CTA order: the K and V of a group's heads (read by
   // every CTA of the head) should stay in L2 while the group runs, ~48 MB
   const double kv_head = 4.0 * (double)p.N * (double)p.hd;
   p.head_group = (int)std::max(1.0, std::min((double)BH, (48.0 * 1024 * 1024) / kv_head));
   constexpr uint32_t smem = fattn::D256Cfg::SMEM_BYTES;
+  const bool split = p.n_splits > 1;
   mark_kernel_start(stream);
-  if (full)
-    fattn::fattn_fwd_d256_kernel<true><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+  if (full && split)
+    fattn::fattn_fwd_d256_kernel<true, true><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+  else if (full)
+    fattn::fattn_fwd_d256_kernel<true, false><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+  else if (split)
+    fattn::fattn_fwd_d256_kernel<false, true><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
   else
-    fattn::fattn_fwd_d256_kernel<false><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
+    fattn::fattn_fwd_d256_kernel<false, false><<<(unsigned)ctas, fattn::D256_THREADS, smem, stream>>>(mq, mk, mv, p);
   mark_kernel_stop(stream);
-  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  if (split) {
+    constexpr int rows_per_block = fattn::COMBINE_THREADS / (fattn::D256 / 16);
+    const dim3 cgrid((unsigned)((p.N + rows_per_block - 1) / rows_per_block), (unsigned)(BH < 65535 ? BH : 65535));
+    fattn::fattn_splitkv_combine_kernel<fattn::D256><<<cgrid, fattn::COMBINE_THREADS, 0, stream>>>(
+        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.hd, p.causal, p.n_splits, fattn::BM,
+        fattn::D256_BN);
+    if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  }
+  return FATTN_OK;
 }
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
@@ -542,7 +578,6 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
   if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
-  if (d > 128 && splits_requested > 1) return FATTN_ERR_UNSUPPORTED;  // no split-KV above 128 columns
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
       (key_len && !aligned(key_len, 4)))
@@ -572,7 +607,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.causal = causal ? 1 : 0;
   p.n_qblocks = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
   p.n_kv_tiles = (N + fattn::BN - 1) / fattn::BN;
-  p.n_splits = d > 128 ? 1 : plan_splits(B, H, N, p.causal, ds->num_sms, splits_requested);
+  p.n_splits = d > 128 ? plan_splits_d256(B, H, N, ds->num_sms, splits_requested)
+                       : plan_splits(B, H, N, p.causal, ds->num_sms, splits_requested);
   const long long units = (long long)B * H * p.n_qblocks * p.n_splits;
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;

@@ -73,7 +73,11 @@ struct D256Cfg {
   static_assert(SMEM_BYTES <= 232448u, "shared memory");
 };
 
-template <bool FULL>
+// SPLIT: p.n_splits > 1 CTAs per query tile, split s taking the run
+// [s*n/n_splits, (s+1)*n/n_splits) of the n key tiles the query tile visits
+// and writing its normalised partial output and log-sum-exp in fp32 for the
+// combine kernel (a row with no visible key in the run: O = 0, -inf).
+template <bool FULL, bool SPLIT>
 __global__ void __launch_bounds__(D256_THREADS, 1)
     fattn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, const Params p) {
@@ -95,10 +99,13 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
   const int BH = p.B * p.H;
   const int n_qt = (p.N + BM - 1) / BM;
   const int u = (int)blockIdx.x;
+  const int ns = SPLIT ? p.n_splits : 1;
+  const int split = SPLIT ? u % ns : 0;
+  const int ub = SPLIT ? u / ns : u;  // the query tile's unit (the splits of one tile are neighbours)
   const int per_group = p.head_group * n_qt;
-  const int g0 = (u / per_group) * p.head_group;
+  const int g0 = (ub / per_group) * p.head_group;
   const int gsz = min(p.head_group, BH - g0);
-  const int rem = u % per_group;
+  const int rem = ub % per_group;
   const int bh = g0 + rem % gsz;
   const int it_rev = rem / gsz;
   const int it = p.causal ? n_qt - 1 - it_rev : it_rev;
@@ -107,7 +114,9 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
   kl = kl < 0 ? 0 : (kl > p.N ? p.N : kl);
   const int max_lim = p.causal ? min(kl, row0 + BM) : kl;
   const int min_lim = p.causal ? min(kl, row0 + 1) : kl;
-  const int n = max_lim > 0 ? (max_lim + D256_BN - 1) / D256_BN : 0;  // key tiles visited
+  const int n_all = max_lim > 0 ? (max_lim + D256_BN - 1) / D256_BN : 0;  // key tiles the query tile visits
+  const int j0 = split * n_all / ns;                                      // this CTA's run of them:
+  const int n = (split + 1) * n_all / ns - j0;                            // tiles j0 .. j0 + n - 1
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q_FULL), 1);
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
 #pragma unroll
         for (int pn = 0; pn < 4; ++pn)
           tma_load_3d(base + C::K_OFF + s * C::KV_BYTES + pn * C::KV_PANEL, &tmap_k, bar(C::B_K_FULL + s), 64 * pn,
-                      j * D256_BN, bh);
+                      (j0 + j) * D256_BN, bh);
         ++kk;
         ok = wait_bar(waiter, bar(C::B_V_EMPTY + s), ph, C::B_V_EMPTY + s, u);
         if (!ok) break;
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
 #pragma unroll
         for (int pn = 0; pn < 4; ++pn)
           tma_load_3d(base + C::V_OFF + s * C::KV_BYTES + pn * C::KV_PANEL, &tmap_v, bar(C::B_V_FULL + s), 64 * pn,
-                      j * D256_BN, bh);
+                      (j0 + j) * D256_BN, bh);
         ++vv;
       }
       // drain: copies that may still be in flight after an abort
@@ -224,7 +233,8 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
       }
       for (int j = 0; ok && j < n; ++j) {
         const int s = j % C::SLOTS;
-        const uint32_t idesc_pv = __ldg(modes + (j * D256_BN) / BN) == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
+        const uint32_t idesc_pv =
+            __ldg(modes + ((j0 + j) * D256_BN) / BN) == VMODE_F16 ? IDESC_PV_F16 : IDESC_PV_BF16;
         ok = wait_bar(waiter, bar(C::B_P_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u, C::B_P_FULL + (j & 1), u);
         if (ok) ok = wait_bar(waiter, bar(C::B_V_FULL + s), (uint32_t)(j / C::SLOTS) & 1u, C::B_V_FULL + s, u);
         ok = __all_sync(0xffffffffu, ok);
@@ -263,8 +273,9 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
     const uint32_t o_addr = tmem + lane_off + D256_TMEM_O;
     const float c = p.scale_log2;
     if (n == 0) {
-      // no visible key: O = 0, LSE = -inf
-      if (row_ok) {
+      // no visible key: O = 0, LSE = -inf (an empty split run writes
+      // nothing: the combine reads only the runs that hold key tiles)
+      if (!SPLIT && row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * hd);
         for (int i = 0; i < hd / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
         p.lse[row_flat] = -INFINITY;
@@ -276,13 +287,13 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         const uint32_t s_addr = tmem + lane_off + D256_TMEM_S + 64u * (uint32_t)(j & 1);
-        const int vmode = __ldg(modes + (j * D256_BN) / BN);
+        const int vmode = __ldg(modes + ((j0 + j) * D256_BN) / BN);
         ok = wait_bar(waiter, bar(C::B_S_FULL + (j & 1)), (uint32_t)(j >> 1) & 1u, C::B_S_FULL + (j & 1), u);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const bool masked_tile = (j + 1) * D256_BN > min_lim;
-        const int vis_n = lim - j * D256_BN;  // columns [0, vis_n) visible
+        const bool masked_tile = (j0 + j + 1) * D256_BN > min_lim;
+        const int vis_n = lim - (j0 + j) * D256_BN;  // columns [0, vis_n) visible
         // S row of this tile; its max from the TMEM load's max reduction when
         // no column is masked, else over the visible columns (tree order)
         float sr[64];
@@ -318,7 +329,9 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
           m_ref = m_new;
           rescale = true;
         }
-        const float mc = m_ref * c;
+        // (a split run can hold rows with no visible key yet: m stays -inf
+        // and every p of theirs is masked to 0)
+        const float mc = m_ref == -INFINITY ? 0.0f : m_ref * c;
         // p = 2^(s*c - m*c) (packed f32x2 FMA, then ex2), masked entries
         // exactly 0; l from the unrounded p in four packed partial sums; P
         // rounded to the V tile's operand type
@@ -395,7 +408,29 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
         ok = wait_bar(waiter, bar(C::B_O_FULL), 0, C::B_O_FULL, u);
         ok = __all_sync(0xffffffffu, ok);
       }
-      if (ok) {
+      if (ok && SPLIT) {
+        // this run's O / l and log-sum-exp in fp32, for the combine kernel
+        // (O = 0 and -inf for a row with no visible key in the run)
+        tc_fence_after();
+        const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+        const size_t orow = (size_t)split * (size_t)BH * (size_t)p.N + row_flat;
+        float4* dstf = reinterpret_cast<float4*>(p.o_part + orow * hd);
+#pragma unroll 1
+        for (int hcol = 0; hcol < D256 / 64; ++hcol) {
+          uint32_t ov[64];
+          tmem_ld64(o_addr + 64u * hcol, ov);
+          tmem_ld_wait(ov);
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (64 * hcol + 4 * i < hd)
+                dstf[16 * hcol + i] =
+                    make_float4(__uint_as_float(ov[4 * i]) * inv_l, __uint_as_float(ov[4 * i + 1]) * inv_l,
+                                __uint_as_float(ov[4 * i + 2]) * inv_l, __uint_as_float(ov[4 * i + 3]) * inv_l);
+          }
+        }
+        if (row_ok) p.lse_part[orow] = l > 0.0f ? (m_ref * c + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      } else if (ok) {
         tc_fence_after();
         const float inv_l = 1.0f / l;
         uint4* dst = reinterpret_cast<uint4*>(p.o + row_flat * hd);

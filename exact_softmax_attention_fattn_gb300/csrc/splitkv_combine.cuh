@@ -9,12 +9,15 @@
 // the outputs weighted the same way), written in terms of L_s = m_s + log l_s:
 //     L = log sum_s e^(L_s),   O = sum_s e^(L_s - L) O_s.
 // Only the splits whose run meets the key tiles of the row's 128-row query
-// tile wrote a partial (each such split holds a visible key for every row of
-// the tile); the runs and tile counts are the attention kernel's: the block
-// of 256 query rows visits n_blk key tiles (those of its later tile), split
-// s takes tiles [s*n_blk/n_splits, (s+1)*n_blk/n_splits), and the row's tile
-// visits the first n_t of them.  A row with no visible key gets O = 0 and
-// LSE = -inf.
+// tile wrote a partial; the runs and tile counts are the attention kernel's:
+// a block of blk_rows query rows (256 for the two-tile kernel, 128 for the
+// head-dim-256 kernel) visits n_blk key tiles of key_tile keys (128, or 64),
+// split s takes tiles [s*n_blk/n_splits, (s+1)*n_blk/n_splits), and the
+// row's 128-row tile visits the first n_t of them.  (With 128-key tiles every
+// such split holds a visible key for every row of the tile; with 64-key
+// tiles a split may hold none for some rows, which then carry O = 0 and
+// L = -inf and weigh nothing; the first split always holds key 0.)  A row
+// with no visible key at all gets O = 0 and LSE = -inf.
 //
 // HBM-bound: per row, (splits with a partial) * (D * 4 + 4) bytes read,
 // D * 2 + 4 written.  Grid (row blocks, heads); D / 16 threads per row, each
@@ -30,11 +33,12 @@ namespace fattn {
 
 constexpr int COMBINE_THREADS = 256;
 
-// Key tiles that query tile `row0` visits (as in the attention kernel).
-__device__ __forceinline__ int combine_tiles_of(int row0, int N, int kl, int causal) {
+// Key tiles of key_tile keys that the 128-row query tile `row0` visits (as
+// in the attention kernel).
+__device__ __forceinline__ int combine_tiles_of(int row0, int N, int kl, int causal, int key_tile) {
   if (row0 >= N) return 0;
   const int max_lim = causal ? min(kl, row0 + 128) : kl;
-  return max_lim > 0 ? (max_lim + 127) / 128 : 0;
+  return max_lim > 0 ? (max_lim + key_tile - 1) / key_tile : 0;
 }
 
 template <int D>
@@ -42,7 +46,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
     fattn_splitkv_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                                  __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                  const int32_t* __restrict__ key_len, int B, int H, int N, int hd, int causal,
-                                 int n_splits) {
+                                 int n_splits, int blk_rows, int key_tile) {
   constexpr int VPT = 4;            // float4 per thread and split
   constexpr int TPR = D / (4 * VPT);  // threads per row (rows of hd <= D columns)
   constexpr int ROWS = COMBINE_THREADS / TPR;
@@ -54,9 +58,10 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     int kl = key_len ? __ldg(key_len + bh / H) : N;
     kl = kl < 0 ? 0 : (kl > N ? N : kl);
-    const int blk0 = row / 256 * 256;
-    const int n_blk = max(combine_tiles_of(blk0, N, kl, causal), combine_tiles_of(blk0 + 128, N, kl, causal));
-    const int n_t = combine_tiles_of(row / 128 * 128, N, kl, causal);
+    const int blk0 = row / blk_rows * blk_rows;
+    int n_blk = 0;
+    for (int r0 = blk0; r0 < blk0 + blk_rows; r0 += 128) n_blk = max(n_blk, combine_tiles_of(r0, N, kl, causal, key_tile));
+    const int n_t = combine_tiles_of(row / 128 * 128, N, kl, causal, key_tile);
     const size_t rg = (size_t)bh * N + row;
     uint2* dst = reinterpret_cast<uint2*>(o + rg * hd) + c4;
     if (n_t == 0) {

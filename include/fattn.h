@@ -48,7 +48,7 @@ typedef enum {
   FATTN_OK = 0,
   FATTN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or scale is invalid */
   FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration the library runs (head dim,
-                                split-KV or backward above head dim 128, no-alloc size) */
+                                backward above head dim 128, no-alloc size) */
   FATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FATTN_ERR_TIMEOUT = 4      /* a bounded wait inside the kernel gave up (see fattn_last_error) */
 } fattn_status;
@@ -157,9 +157,14 @@ FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void*
  *             combine kernel:
  *                 LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
  *             over the splits that hold keys of the row.
- *             Negative: FATTN_ERR_INVALID_ARG.  Above head dim 128 only 0
- *             and 1 are accepted (the 256-column kernel never splits); k > 1
- *             there returns FATTN_ERR_UNSUPPORTED before anything is enqueued.
+ *             Above head dim 128 the 256-column kernel works on one 128-row
+ *             query tile per CTA and on key tiles of 64: k > 1 gives
+ *             min(k, ceil(N/64)) splits, cutting the n key tiles of 64 that
+ *             the query tile visits in the same way, merged by the same rule
+ *             (a split may hold no visible key for some rows of its tile:
+ *             those carry O_s = 0 and LSE_s = -inf and weigh nothing).
+ *             Negative: FATTN_ERR_INVALID_ARG.  Head dims as for fattn_fwd
+ *             at every split count: multiples of 8 from 8 to 256.
  *
  * Every other argument, the layouts, ownership and errors are those of
  * fattn_fwd (head dims: multiples of 8 from 8 to 256); the scratch is as

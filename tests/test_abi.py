@@ -254,10 +254,10 @@ def _decl_comment(name: str) -> str:
 def _stated_max_head_dim(name: str, split: bool = False) -> int:
     """The largest head dim the header states for an entry point ('a multiple
     of 8 from 8 to D'); for fattn_fwd_splitkv with split=True, the bound it
-    states for k > 1 splits ('Above head dim D only 0 and 1')."""
+    states for k > 1 splits ('at every split count: multiples of 8 from 8 to D')."""
     c = " ".join(_decl_comment(name).split())
     if split:
-        return int(re.search(r"Above head dim (\d+) only 0 and 1", c).group(1))
+        return int(re.search(r"at every split count: multiples of 8 from 8 to (\d+)", c).group(1))
     m = re.search(r"multiples? of 8 from 8 to (\d+)", c)
     assert m, f"{name}: the header states no head-dim range"
     return int(m.group(1))

@@ -30,6 +30,7 @@ from exact_softmax_attention_fattn_gb300.inputs import Workload, make_inputs
 # shapes whose waits run well past 1 us: the 256-column kernel, whose CTAs
 # each hold one query tile, gets a non-causal problem (every CTA 64 key tiles)
 shapes = {"fwd": (1, 4, 2048, 128, True), "split": (1, 2, 4096, 128, True), "d256": (1, 8, 4096, 256, False),
+          "d256split": (1, 2, 4096, 256, False),
           "bwd": (1, 2, 1024, 128, True), "noalloc": (1, 4, 2048, 128, True), "linear": (2, 4, 4096, 64, True)}
 B, H, N, d, causal = shapes[case]
 x = make_inputs(Workload("to", B, H, N, d, causal, 50))
@@ -51,7 +52,7 @@ elif case == "noalloc":
                               1.0 / d ** 0.5, int(causal), None, torch.cuda.current_stream().cuda_stream)
     assert st0 == 0, st0
 else:
-    binding.forward_into(q, k, v, o, lse, causal=causal, n_splits=4 if case == "split" else None)
+    binding.forward_into(q, k, v, o, lse, causal=causal, n_splits=4 if case in ("split", "d256split") else None)
 st, detail = binding.last_error()
 again, _ = binding.last_error()          # the flag is cleared once read
 a = torch.randn(512, 512, device=dev)
@@ -61,7 +62,7 @@ print(json.dumps({"status": st, "detail": detail, "again": again, "context_ok": 
 """
 
 
-@pytest.mark.parametrize("case", ["fwd", "split", "d256", "bwd", "noalloc", "linear"])
+@pytest.mark.parametrize("case", ["fwd", "split", "d256", "d256split", "bwd", "noalloc", "linear"])
 def test_bounded_wait_times_out_and_reports(cuda_device, case):
     """Each kernel family (the forward, its split-KV instantiation, the
     256-column forward, the backward's kernels, the tensor-core linear

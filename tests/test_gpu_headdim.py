@@ -4,9 +4,11 @@ A head dim d (a multiple of 8) runs in the 64- or 128-column kernels (d <=
 128) or the one-query-tile 256-column kernel (136..256), with the columns
 past d read as zeros by the tensor maps: they add nothing to Q K^T, give
 zero output columns that are never stored, and the rows in memory stay d
-elements long.  Forward (unsplit and, up to 128, split-KV) at the forward's
-bars, backward (up to 128) at the derived gradient bar, with poisoned guard
-bands around the outputs.
+elements long.  Forward (unsplit and split-KV) at the forward's bars,
+backward (up to 128) at the derived gradient bar, with poisoned guard bands
+around the outputs.  Small problems at d > 128 split the key range on their
+own (fewer query tiles than SMs), so the plain large-d cases below run the
+split path too.
 """
 from __future__ import annotations
 
@@ -113,7 +115,21 @@ def test_forward_d256_long(cuda_device):
     compare(o_g.reshape(-1, 256)[rows], l_g.reshape(-1)[rows], o_r, l_r, "d=256 N=4096 causal")
 
 
-def test_large_head_dims_refuse_split_and_backward(cuda_device):
+@pytest.mark.parametrize("d", [136, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_large_head_dims_split(cuda_device, d, causal):
+    """Explicit split counts at d > 128 (runs of 64-key tiles, fp32 partials,
+    the combine), with key padding that leaves some runs empty and some rows
+    with no visible key in a run: kl = 0 (nothing visible), 1, 65, 700."""
+    x = make_inputs(Workload("hd_large_split", 4, 2, 700, d, causal, 950 + d, qk_sigma=2.0))
+    kl = [0, 1, 65, 700]
+    o_r, l_r = oracle.forward(x.q, x.k, x.v, x.w.softmax_scale, causal, key_len=kl)
+    for n_splits in (1, 2, 3, 11):
+        o_g, l_g = run_gpu(x, cuda_device, key_len=kl, n_splits=n_splits)
+        compare(o_g, l_g, o_r, l_r, f"d={d} causal={causal} key_len splits={n_splits}")
+
+
+def test_large_head_dims_refuse_backward(cuda_device):
     import torch
 
     from exact_softmax_attention_fattn_gb300 import binding
@@ -123,10 +139,7 @@ def test_large_head_dims_refuse_split_and_backward(cuda_device):
     q, k, v = (bits_to_device(a, cuda_device) for a in (x.q, x.k, x.v))
     o = torch.empty_like(q)
     lse = torch.empty((1, 1, 256), dtype=torch.float32, device=cuda_device)
-    with pytest.raises(binding.FattnError) as e:
-        binding.forward_into(q, k, v, o, lse, n_splits=2)
-    assert e.value.status == binding.FATTN_ERR_UNSUPPORTED
-    binding.forward_into(q, k, v, o, lse, n_splits=1)  # one split is the plain forward
+    binding.forward_into(q, k, v, o, lse, n_splits=1)
     with pytest.raises(binding.FattnError) as e:
         binding.backward(q, k, v, o, lse, q)
     assert e.value.status == binding.FATTN_ERR_UNSUPPORTED
