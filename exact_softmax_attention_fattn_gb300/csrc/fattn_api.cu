@@ -14,6 +14,7 @@
 
 #include "../../include/fattn.h"
 #include "fattn_bwd.cuh"
+#include "fattn_bwd256.cuh"
 #include "fattn_d256.cuh"
 #include "fattn_kernel.cuh"
 #include "linear_attn.cuh"
@@ -84,6 +85,19 @@ int configure_fwd_kernel() {
   if (cudaFuncGetAttributes(&a, fattn::fattn_fwd_kernel<D, SPLIT, FULL>) != cudaSuccess) return FATTN_ERR_CUDA;
   if (a.numRegs != fattn::LAUNCH_REGS) return FATTN_ERR_UNSUPPORTED;
   return FATTN_OK;
+}
+
+// The three passes of the 256-column backward.
+int configure_bwd256_kernels() {
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  return cudaFuncSetAttribute(fattn::fattn_bwd256_kernel<fattn::BP_DV>, attr,
+                              (int)fattn::Bwd256Cfg<fattn::BP_DV>::SMEM_BYTES) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_bwd256_kernel<fattn::BP_DK>, attr,
+                                      (int)fattn::Bwd256Cfg<fattn::BP_DK>::SMEM_BYTES) == cudaSuccess &&
+                 cudaFuncSetAttribute(fattn::fattn_bwd256_kernel<fattn::BP_DQ>, attr,
+                                      (int)fattn::Bwd256Cfg<fattn::BP_DQ>::SMEM_BYTES) == cudaSuccess
+             ? FATTN_OK
+             : FATTN_ERR_CUDA;
 }
 
 template <bool FULL>
@@ -171,6 +185,7 @@ int device_state(int dev, DeviceState** out) {
     if (rc == FATTN_OK) rc = configure_kernel<128>();
     if (rc == FATTN_OK) rc = configure_d256_kernel<true>();
     if (rc == FATTN_OK) rc = configure_d256_kernel<false>();
+    if (rc == FATTN_OK) rc = configure_bwd256_kernels();
     if (rc == FATTN_OK) rc = configure_linear_kernels();
     if (rc != FATTN_OK) return rc;
     if (!s.pool && make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
@@ -297,8 +312,8 @@ int encode_map_f32(CUtensorMap* map, const void* ptr, int BH, int N, int F) {
 
 // Head dims the kernels run: multiples of 8 (rows of 16-byte vectors, TMA
 // strides in 16-byte units), computed in the 64-, 128- or 256-column kernel
-// with the columns past d read as zeros by the tensor maps.  The forward runs
-// up to 256, the backward up to 128.
+// with the columns past d read as zeros by the tensor maps.  The forward and
+// the backward run up to 256.
 bool head_dim_supported(int d, int max_d = 256) { return d >= 8 && d <= max_d && d % 8 == 0; }
 
 // Scratch of one call: V in its per-tile storage type, then one mode byte per
@@ -947,6 +962,48 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
   return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+// Head dims 136..256: the prep kernel, then the dV, dK and dQ passes of the
+// 256-column backward (fattn_bwd256.cuh).
+int enqueue_bwd256(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                   fattn::BwdParams p, float* rows, cudaStream_t stream) {
+  const int BH = p.B * p.H;
+  const long long n_rows = (long long)BH * p.N_pad;
+  float* lse2 = rows;
+  float* delta = rows + n_rows;
+  p.lse2 = lse2;
+  p.delta = delta;
+  constexpr int D = fattn::D256;
+  const long long prep_threads = n_rows * (D / 8);
+  const unsigned prep_blocks = (unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS);
+  if (p.hd == D)
+    fattn::fattn_bwd_prep_kernel<D, true><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        n_rows);
+  else
+    fattn::fattn_bwd_prep_kernel<D, false><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        n_rows);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo;
+  if (encode_map(&mq, q, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mv, v, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mdo, dout, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
+    return FATTN_ERR_CUDA;
+  const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
+  fattn::fattn_bwd256_kernel<fattn::BP_DV>
+      <<<grid, fattn::BWD_THREADS, fattn::Bwd256Cfg<fattn::BP_DV>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  mark_kernel_start(stream);
+  fattn::fattn_bwd256_kernel<fattn::BP_DK>
+      <<<grid, fattn::BWD_THREADS, fattn::Bwd256Cfg<fattn::BP_DK>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  mark_kernel_stop(stream);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  fattn::fattn_bwd256_kernel<fattn::BP_DQ>
+      <<<grid, fattn::BWD_THREADS, fattn::Bwd256Cfg<fattn::BP_DQ>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -957,7 +1014,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   if (!std::isfinite(scale) || scale < 0.0f) return FATTN_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
-  if (!head_dim_supported(d, 128)) return FATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d)) return FATTN_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7FFFFFFFll || N > 0x7FFFFFFF - 512) return FATTN_ERR_INVALID_ARG;
   const void* ptrs16[8] = {q, k, v, o, dout, dq, dk, dv};
   for (const void* ptr : ptrs16)
@@ -998,7 +1055,9 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
     return FATTN_ERR_CUDA;
   }
   float* rf = reinterpret_cast<float*>(rows);
-  rc = d <= 64 ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s) : enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s);
+  rc = d <= 64    ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s)
+       : d <= 128 ? enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s)
+                  : enqueue_bwd256(q, k, v, o, dout, lse, p, rf, s);
   if (cudaFreeAsync(rows, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }

@@ -274,6 +274,36 @@ __device__ __forceinline__ void mma_ts_batch8(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// The same over 128 keys with A packed per 64-key half: keys 64h..64h+63 in
+// TMEM columns 64h..64h+31 (two groups of threads, each packing its own half).
+__device__ __forceinline__ void mma_ts_batch8_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 blo, bhi, bl, at;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 bl, blo, 128;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 256;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 16;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 384;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 24;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 512;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 64;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 640;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 72;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 768;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 80;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 896;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 88;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // TS form with the B descriptor advanced by OFF and the A TMEM column by ACOL.
 template <uint32_t OFF, uint32_t ACOL>
 __device__ __forceinline__ void mma_ts_w_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,

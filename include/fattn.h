@@ -48,7 +48,7 @@ typedef enum {
   FATTN_OK = 0,
   FATTN_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or scale is invalid */
   FATTN_ERR_UNSUPPORTED = 2, /* valid, but not a configuration the library runs (head dim,
-                                backward above head dim 128, no-alloc size) */
+                                no-alloc size) */
   FATTN_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   FATTN_ERR_TIMEOUT = 4      /* a bounded wait inside the kernel gave up (see fattn_last_error) */
 } fattn_status;
@@ -125,18 +125,22 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
  *   dout     dL/dO, bf16 [B, H, N, d].
  *   dq, dk, dv  written: bf16 [B, H, N, d]; each rounded once from fp32.
  *   B, H, N, scale, causal, key_len, stream: as for fattn_fwd.
- *   d        head dim: a multiple of 8 from 8 to 128 (the backward has no
- *            256-column kernel; 136..256 return FATTN_ERR_UNSUPPORTED).
+ *   d        head dim: a multiple of 8 from 8 to 256.  Up to 128 one
+ *            kernel forms dK and dV together and another dQ; from 136 the
+ *            256-column accumulators leave room for one of them at a time in
+ *            tensor memory, so dV, dK and dQ each take a pass of their own
+ *            (S recomputed in each, dP in the last two).
  *
  * A query row with no visible key gets dQ = 0; a key visible to no query
  * (key_len) gets dK = dV = 0.  All device pointers 16-byte aligned (lse and
  * key_len 4-byte); the caller owns every tensor.  Each call takes
  * 2 * B*H*ceil(N/128)*128 * 4 bytes of scratch from the library's pool on
  * `stream` (per-row D and LSE in base 2) and returns it in stream order;
- * it enqueues three kernels on `stream` and returns without synchronising.
+ * it enqueues three kernels (four from head dim 136) on `stream` and returns
+ * without synchronising.
  *
  * Returns FATTN_OK, FATTN_ERR_INVALID_ARG, FATTN_ERR_UNSUPPORTED (d not a
- * multiple of 8 in [8, 128]) or FATTN_ERR_CUDA, with argument errors detected before anything
+ * multiple of 8 in [8, 256]) or FATTN_ERR_CUDA, with argument errors detected before anything
  * is enqueued; time-outs of the kernels' bounded waits are reported by
  * fattn_last_error().
  */

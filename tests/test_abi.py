@@ -136,8 +136,7 @@ def test_backward_argument_checks(lib):
         assert bcall(**{name: FAKE + 8}) == binding.FATTN_ERR_INVALID_ARG, name
     assert bcall(lse=FAKE + 2) == binding.FATTN_ERR_INVALID_ARG
     assert bcall(d=100) == binding.FATTN_ERR_UNSUPPORTED
-    assert bcall(d=136) == binding.FATTN_ERR_UNSUPPORTED  # the backward runs head dims up to 128
-    assert bcall(d=256) == binding.FATTN_ERR_UNSUPPORTED
+    assert bcall(d=264) == binding.FATTN_ERR_UNSUPPORTED  # the backward runs head dims up to 256
     buf = np.zeros(128 * 64 * 4, dtype=np.uint8)
     addr = buf.ctypes.data + (-buf.ctypes.data) % 16
     host = {n: addr for n in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv")}
@@ -296,7 +295,7 @@ def test_header_head_dim_ranges_match_the_library(lib):
             assert fn(d) == binding.FATTN_ERR_UNSUPPORTED, (name, d)
     # the forward's own statement of its range
     assert _stated_max_head_dim("fattn_fwd") == 256
-    assert _stated_max_head_dim("fattn_bwd") == 128
+    assert _stated_max_head_dim("fattn_bwd") == 256
 
 
 def test_status_codes_cite_their_convention():

@@ -5,8 +5,8 @@ A head dim d (a multiple of 8) runs in the 64- or 128-column kernels (d <=
 past d read as zeros by the tensor maps: they add nothing to Q K^T, give
 zero output columns that are never stored, and the rows in memory stay d
 elements long.  Forward (unsplit and split-KV) at the forward's bars,
-backward (up to 128) at the derived gradient bar, with poisoned guard bands
-around the outputs.  Small problems at d > 128 split the key range on their
+backward at the derived gradient bar (from 136 the three-pass 256-column
+backward), with poisoned guard bands around the outputs.  Small problems at d > 128 split the key range on their
 own (fewer query tiles than SMs), so the plain large-d cases below run the
 split path too.
 """
@@ -70,7 +70,7 @@ def guarded_backward(x, g, dev, causal, scale):
     return tuple(t.float().cpu().numpy().astype(np.float64) for t in grads)
 
 
-@pytest.mark.parametrize("d", [16, 32, 96, 120])
+@pytest.mark.parametrize("d", [16, 32, 96, 120, 136, 192, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_head_dims(cuda_device, d, causal):
     x = make_inputs(Workload("hd_bwd", 2, 2, 300, d, causal, 700 + d))
@@ -129,17 +129,32 @@ def test_forward_large_head_dims_split(cuda_device, d, causal):
         compare(o_g, l_g, o_r, l_r, f"d={d} causal={causal} key_len splits={n_splits}")
 
 
-def test_large_head_dims_refuse_backward(cuda_device):
+@pytest.mark.parametrize("d", [200, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_large_head_dims_key_padding(cuda_device, d, causal):
+    """The 256-column backward with key lengths {0, 1, 129, 300}: a batch
+    entry with no visible key (dQ = dK = dV = 0 there), keys past key_len
+    (dK = dV = 0), N = 300 ragged over three 128-row tiles, Q, K ~ N(0, 2^2)."""
     import torch
 
     from exact_softmax_attention_fattn_gb300 import binding
     from tests.gpu_helpers import bits_to_device
 
-    x = make_inputs(Workload("hd256_refuse", 1, 1, 256, 256, False, 903))
-    q, k, v = (bits_to_device(a, cuda_device) for a in (x.q, x.k, x.v))
+    B, H, N = 4, 1, 300
+    x = make_inputs(Workload("hd_bwd_kl", B, H, N, d, causal, 960 + d, qk_sigma=2.0))
+    g = make_inputs(Workload("hd_bwd_kl_g", B, H, N, d, causal, 1960 + d)).v
+    kl = np.array([0, 1, 129, 300], np.int32)
+    scale = 1.0 / np.sqrt(d)
+    dev = cuda_device
+    q, k, v, go = (bits_to_device(a, dev) for a in (x.q, x.k, x.v, g))
+    kl_t = torch.from_numpy(kl).to(dev)
     o = torch.empty_like(q)
-    lse = torch.empty((1, 1, 256), dtype=torch.float32, device=cuda_device)
-    binding.forward_into(q, k, v, o, lse, n_splits=1)
-    with pytest.raises(binding.FattnError) as e:
-        binding.backward(q, k, v, o, lse, q)
-    assert e.value.status == binding.FATTN_ERR_UNSUPPORTED
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    binding.forward_into(q, k, v, o, lse, causal=causal, scale=scale, key_len=kl_t)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    binding.backward_into(q, k, v, o, lse, go, dq, dk, dv, causal=causal, scale=scale, key_len=kl_t)
+    st, detail = binding.last_error()
+    assert st == binding.FATTN_OK, detail
+    ours = tuple(t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+    ref = oracle.backward(x.q, x.k, x.v, g, scale, causal, key_len=kl)
+    check_grads(ours, ref, f"backward d={d} causal={causal} key_len")
