@@ -93,6 +93,8 @@ CSRC = os.path.join(ROOT, "exact_softmax_attention_fattn_gb300", "csrc")
 
 KERNEL_SOURCES = ("fattn_kernel.cuh", "ptx.cuh")
 BWD_SOURCES = ("fattn_bwd.cuh", "ptx.cuh")
+BWD256_SOURCES = ("fattn_bwd256.cuh", "fattn_bwd.cuh", "ptx.cuh")
+D256_SOURCES = ("fattn_d256.cuh", "ptx.cuh")
 LINEAR_SOURCES = ("linear_tc.cuh", "ptx.cuh")
 
 
@@ -470,13 +472,16 @@ def our_arm(args, rank: int, world: int, local_rank: int):
     peak, peak_kind, hbm_gbs = measured_peaks()
     # the dominant kernel (the attention kernel) on its own CUDA-event time
     attn_mean_ms = float(np.mean(attn_ms))
-    traffic = ncu_traffic(args.workload)
+    # head dims above 128 run the 256-column kernel, profiled under its own name
+    prof_name, prof_src = ((f"fattn_fwd_d256_kernel_{args.workload}", D256_SOURCES) if w.d > 128 else
+                           (KERNEL_NAME + "_" + args.workload, KERNEL_SOURCES))
+    traffic = ncu_traffic(args.workload, prof_name, prof_src)
     roof = forward_roofline(flops, algorithmic_bytes(w, x.key_len), attn_mean_ms, ms_per_step, peak, peak_kind,
                             hbm_gbs, (clocks or {}).get("sm_mhz"), sms)
     roof.update({"traffic": traffic if n_splits == 1 else None,
                  "kernel": "attention kernel alone (V pre-pass and split-KV combine excluded)",
                  "kernel_ms_mean": attn_mean_ms})
-    tpa = profile_field(KERNEL_NAME + "_" + args.workload, "tensor_pipe_active_pct_of_active")
+    tpa = profile_field(prof_name, "tensor_pipe_active_pct_of_active", prof_src)
     if tpa:
         roof["ncu_tensor_pipe_active_pct"] = float(tpa.split()[0])
     cpu = None
@@ -732,9 +737,12 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
     if rank != 0:
         return
     peak, peak_kind, _ = measured_peaks()
-    # the dominant kernel (dK/dV: S, dP, dV, dK = 4 of the forward's 2 GEMMs) on its own CUDA-event time
+    # the dominant kernel on its own CUDA-event time: up to head dim 128 the
+    # dK/dV kernel (S, dP, dV, dK = 4 of the forward's 2 GEMMs), above it the
+    # dK pass of the three-pass backward (S, dP, dK = 3)
+    big = w.d > 128
     dkdv_mean_ms = float(np.mean(dkdv_ms))
-    achieved = (flops / 2.5 * 2.0) / (dkdv_mean_ms * 1e-3) / 1e12
+    achieved = (flops / 2.5 * (1.5 if big else 2.0)) / (dkdv_mean_ms * 1e-3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         # the fp64 oracle backward on one head (about 2.5x the head's forward FLOPs)
@@ -755,15 +763,17 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "traffic": ncu_traffic(args.workload, f"fattn_bwd_kernels_{args.workload}", BWD_SOURCES,
-                                            "dkdv_dram_bytes_per_launch"),
-                     "kernel": "dK/dV kernel alone (its 4 GEMMs: 2x the forward's FLOPs)",
+                     "traffic": ncu_traffic(args.workload, f"fattn_bwd_kernels_{args.workload}",
+                                            BWD256_SOURCES if big else BWD_SOURCES, "dkdv_dram_bytes_per_launch"),
+                     "kernel": ("dK pass alone (its 3 GEMMs: 1.5x the forward's FLOPs)" if big else
+                                "dK/dV kernel alone (its 4 GEMMs: 2x the forward's FLOPs)"),
                      "kernel_ms_mean": dkdv_mean_ms},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,  # prep + dK/dV + dQ kernels per step
-        "kernel": "fattn_bwd_prep_kernel + fattn_bwd_dkdv_kernel + fattn_bwd_dq_kernel",
+        "gpu_launches": (4 if big else 3) * args.steps,  # prep + dK/dV + dQ kernels (prep + three passes) per step
+        "kernel": ("fattn_bwd_prep_kernel + fattn_bwd256_kernel (dV, dK, dQ passes)" if big else
+                   "fattn_bwd_prep_kernel + fattn_bwd_dkdv_kernel + fattn_bwd_dq_kernel"),
         "kernel_ms": {"min": min(kernel_ms), "median": float(np.median(kernel_ms)), "max": max(kernel_ms)},
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
