@@ -610,6 +610,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
 
   fattn::Params p;
   p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.o_v8 = (aligned(o, 32) && d % 16 == 0) ? 1 : 0;  // rows of O take 32-byte stores
   p.lse = lse;
   p.key_len = key_len;
   p.err = ds->err;
@@ -1157,6 +1158,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
 
   fattn::Params p;
   p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.o_v8 = (aligned(o, 32) && d % 16 == 0) ? 1 : 0;  // rows of O take 32-byte stores
   p.lse = lse;
   p.key_len = key_len;
   p.err = reinterpret_cast<int*>(ns->scratch + kNoAllocScratch);

@@ -92,6 +92,7 @@ struct Params {
   float scale;       // softmax scale (natural units), >= 0
   float scale_log2;  // scale * log2(e)
   int causal;
+  int o_v8;       // O is 32-byte aligned and hd a multiple of 16: rows of O take 32-byte stores
   int n_qblocks;  // ceil(N / 256)
   int n_units;    // B * H * n_qblocks * n_splits
   int n_splits;    // K/V splits per query block (1: no split, O and LSE written directly)
@@ -853,12 +854,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(bar_o_empty);
           }
           if (row_ok) {
-            float4* dstf = reinterpret_cast<float4*>(p.o_part + orow * hd) + 16 * hcol;
+            // 32-byte stores (the partials are the library's own scratch, rows
+            // of hd fp32: 32-byte aligned for every head dim)
+            float* dstf = p.o_part + orow * hd + 64 * hcol;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (64 * hcol + 4 * i < hd)
-                dstf[i] = make_float4(__uint_as_float(ov[4 * i]) * inv_l, __uint_as_float(ov[4 * i + 1]) * inv_l,
-                                      __uint_as_float(ov[4 * i + 2]) * inv_l, __uint_as_float(ov[4 * i + 3]) * inv_l);
+            for (int i = 0; i < 8; ++i)
+              if (64 * hcol + 8 * i < hd)
+                st_global_v8(dstf + 8 * i, __float_as_uint(__uint_as_float(ov[8 * i]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 1]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 2]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 3]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 4]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 5]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 6]) * inv_l),
+                             __float_as_uint(__uint_as_float(ov[8 * i + 7]) * inv_l));
           }
         }
         if (row_ok) p.lse_part[orow] = (m_ref * c + __log2f(l)) * 0.69314718055994531f;  // l > 0 here
@@ -880,10 +889,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(bar_o_empty);
           }
           if (row_ok) {
+            if (p.o_v8) {
+              // 32-byte stores: whole sectors of the row (measured 0.4 % faster
+              // on the b2h16n4096d128 causal call, 2 % with key padding)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (64 * hcol + 8 * i < hd)
-                dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                if (64 * hcol + 16 * i < hd)
+                  st_global_v8(dst + 8 * hcol + 2 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3],
+                               ob[8 * i + 4], ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (64 * hcol + 8 * i < hd)
+                  dst[8 * hcol + i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+            }
           }
         }
         if (row_ok) {

@@ -200,3 +200,28 @@ def test_kernel_event_hook(cuda_device):
     binding.forward_into(q, k, v, o, lse, causal=True)
     torch.cuda.synchronize(cuda_device)
     assert ks.elapsed_time(ke) == t_kernel
+
+
+@pytest.mark.parametrize("off_elems", [0, 8])
+def test_output_alignment_16_and_32_bytes(cuda_device, off_elems):
+    """O at a 32-byte boundary (rows stored 32 bytes at a time) and at an odd
+    16-byte boundary (16-byte stores): the same values."""
+    import torch
+
+    from exact_softmax_attention_fattn_gb300 import binding
+    from tests.gpu_helpers import bits_to_device
+
+    x = make_inputs(Workload("align", 1, 2, 300, 128, True, 41))
+    q, k, v = (bits_to_device(a, cuda_device) for a in (x.q, x.k, x.v))
+    n = q.numel()
+    buf = torch.zeros(n + 64, dtype=torch.int16, device=cuda_device)
+    base = (-buf.data_ptr() // 2) % 16  # first element at a 32-byte boundary
+    o = buf[base + off_elems:base + off_elems + n].view(torch.bfloat16).view(q.shape)
+    assert o.data_ptr() % 32 == (0 if off_elems == 0 else 16)
+    lse = torch.empty((1, 2, 300), dtype=torch.float32, device=cuda_device)
+    binding.forward_into(q, k, v, o, lse, causal=True, scale=x.w.softmax_scale)
+    st, detail = binding.last_error()
+    assert st == binding.FATTN_OK, detail
+    o_r, l_r = oracle.forward(x.q, x.k, x.v, x.w.softmax_scale, True)
+    compare(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), o_r, l_r,
+            f"O offset {off_elems} elements")
