@@ -741,8 +741,10 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
     # dK/dV kernel (S, dP, dV, dK = 4 of the forward's 2 GEMMs), above it the
     # dK pass of the three-pass backward (S, dP, dK = 3)
     big = w.d > 128
+    # the single-kernel backward (FATTN_BWD_FUSED=1, head dims 72..128): all 5 GEMMs
+    fused = os.environ.get("FATTN_BWD_FUSED", "").startswith("1") and 64 < w.d <= 128
     dkdv_mean_ms = float(np.mean(dkdv_ms))
-    achieved = (flops / 2.5 * (1.5 if big else 2.0)) / (dkdv_mean_ms * 1e-3) / 1e12
+    achieved = (flops / 2.5 * (1.5 if big else 2.5 if fused else 2.0)) / (dkdv_mean_ms * 1e-3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         # the fp64 oracle backward on one head (about 2.5x the head's forward FLOPs)
@@ -763,16 +765,20 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "traffic": ncu_traffic(args.workload, f"fattn_bwd_kernels_{args.workload}",
-                                            BWD256_SOURCES if big else BWD_SOURCES, "dkdv_dram_bytes_per_launch"),
+                     "traffic": None if fused else ncu_traffic(args.workload, f"fattn_bwd_kernels_{args.workload}",
+                                                               BWD256_SOURCES if big else BWD_SOURCES,
+                                                               "dkdv_dram_bytes_per_launch"),
                      "kernel": ("dK pass alone (its 3 GEMMs: 1.5x the forward's FLOPs)" if big else
+                                "fused backward kernel alone (its 5 GEMMs: 2.5x the forward's FLOPs)" if fused else
                                 "dK/dV kernel alone (its 4 GEMMs: 2x the forward's FLOPs)"),
                      "kernel_ms_mean": dkdv_mean_ms},
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": (4 if big else 3) * args.steps,  # prep + dK/dV + dQ kernels (prep + three passes) per step
+        # prep + dK/dV + dQ kernels (prep + three passes; prep + fused + dQ conversion, and a memset) per step
+        "gpu_launches": (4 if big else 3) * args.steps,
         "kernel": ("fattn_bwd_prep_kernel + fattn_bwd256_kernel (dV, dK, dQ passes)" if big else
+                   "fattn_bwd_prep_kernel + fattn_bwd_fused_kernel + fattn_bwd_dq_finalize_kernel" if fused else
                    "fattn_bwd_prep_kernel + fattn_bwd_dkdv_kernel + fattn_bwd_dq_kernel"),
         "kernel_ms": {"min": min(kernel_ms), "median": float(np.median(kernel_ms)), "max": max(kernel_ms)},
         "wall_s_timed_region": wall,

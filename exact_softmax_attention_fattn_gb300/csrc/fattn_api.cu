@@ -15,6 +15,7 @@
 #include "../../include/fattn.h"
 #include "fattn_bwd.cuh"
 #include "fattn_bwd256.cuh"
+#include "fattn_bwd_fused.cuh"
 #include "fattn_d256.cuh"
 #include "fattn_kernel.cuh"
 #include "linear_attn.cuh"
@@ -186,6 +187,9 @@ int device_state(int dev, DeviceState** out) {
     if (rc == FATTN_OK) rc = configure_d256_kernel<true>();
     if (rc == FATTN_OK) rc = configure_d256_kernel<false>();
     if (rc == FATTN_OK) rc = configure_bwd256_kernels();
+    if (rc == FATTN_OK && cudaFuncSetAttribute(fattn::fattn_bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)fattn::FusedCfg::SMEM_BYTES) != cudaSuccess)
+      rc = FATTN_ERR_CUDA;
     if (rc == FATTN_OK) rc = configure_linear_kernels();
     if (rc != FATTN_OK) return rc;
     if (!s.pool && make_pool(dev, &s.pool) != FATTN_OK) return FATTN_ERR_CUDA;
@@ -287,6 +291,7 @@ int encode_map(CUtensorMap* map, const void* ptr, int BH, int N, int d, CUtensor
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 
 // [B*H, N, F] fp32 viewed as a 3-D tensor {F, N, B*H}, boxes of 64 x 128 x 1
 // without swizzle (rows of 256 bytes in shared memory); columns past F and
@@ -963,6 +968,54 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
   return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+// Head dims 72..128 in one pass (fattn_bwd_fused.cuh): the prep kernel, the
+// zeroing of the fp32 dQ buffer `dq_acc` ([B*H, N_pad, 128]), the fused
+// kernel and the conversion of dQ to bf16.
+int enqueue_bwd_fused(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                      fattn::BwdParams p, float* rows, float* dq_acc, cudaStream_t stream) {
+  constexpr int D = fattn::FB_D;
+  const int BH = p.B * p.H;
+  const long long n_rows = (long long)BH * p.N_pad;
+  p.lse2 = rows;
+  p.delta = rows + n_rows;
+  p.dq_acc = dq_acc;
+  const long long prep_threads = n_rows * (D / 8);
+  const unsigned prep_blocks = (unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS);
+  if (p.hd == D)
+    fattn::fattn_bwd_prep_kernel<D, true><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, rows, rows + n_rows, p.N,
+        p.N_pad, p.hd, n_rows);
+  else
+    fattn::fattn_bwd_prep_kernel<D, false><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, rows, rows + n_rows, p.N,
+        p.N_pad, p.hd, n_rows);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaMemsetAsync(dq_acc, 0, (size_t)n_rows * D * sizeof(float), stream) != cudaSuccess) return FATTN_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo;
+  if (encode_map(&mq, q, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, fattn::FB_BQ) != FATTN_OK ||
+      encode_map(&mk, k, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mv, v, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK ||
+      encode_map(&mdo, dout, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, fattn::FB_BQ) != FATTN_OK)
+    return FATTN_ERR_CUDA;
+  const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
+  mark_kernel_start(stream);
+  fattn::fattn_bwd_fused_kernel<<<grid, fattn::FB_THREADS, fattn::FusedCfg::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  mark_kernel_stop(stream);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+  const long long n_vec = (long long)BH * p.N * (p.hd / 8);
+  fattn::fattn_bwd_dq_finalize_kernel<<<(unsigned)((n_vec + 255) / 256), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint4*>(p.dq), p.N, p.N_pad, p.hd, p.scale, n_vec);
+  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+bool fused_bwd_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("FATTN_BWD_FUSED");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
 // Head dims 136..256: the prep kernel, then the dV, dK and dQ passes of the
 // 256-column backward (fattn_bwd256.cuh).
 int enqueue_bwd256(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -1047,6 +1100,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   p.wait_limit_ns = wait_limit_ns();
   p.lse2 = nullptr;
   p.delta = nullptr;
+  p.dq_acc = nullptr;
   if ((long long)B * H * p.n_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* rows = nullptr;
@@ -1056,9 +1110,21 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
     return FATTN_ERR_CUDA;
   }
   float* rf = reinterpret_cast<float*>(rows);
-  rc = d <= 64    ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s)
-       : d <= 128 ? enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s)
-                  : enqueue_bwd256(q, k, v, o, dout, lse, p, rf, s);
+  if (d > 64 && d <= 128 && fused_bwd_enabled()) {
+    void* acc = nullptr;
+    if (cudaMallocFromPoolAsync(&acc, (size_t)B * H * (size_t)p.N_pad * fattn::FB_D * sizeof(float), ds->pool, s) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeAsync(rows, s);
+      return FATTN_ERR_CUDA;
+    }
+    rc = enqueue_bwd_fused(q, k, v, o, dout, lse, p, rf, reinterpret_cast<float*>(acc), s);
+    if (cudaFreeAsync(acc, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
+  } else {
+    rc = d <= 64    ? enqueue_bwd<64>(q, k, v, o, dout, lse, p, rf, s)
+         : d <= 128 ? enqueue_bwd<128>(q, k, v, o, dout, lse, p, rf, s)
+                    : enqueue_bwd256(q, k, v, o, dout, lse, p, rf, s);
+  }
   if (cudaFreeAsync(rows, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   return rc;
 }

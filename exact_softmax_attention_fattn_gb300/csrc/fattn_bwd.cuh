@@ -52,6 +52,7 @@ struct BwdParams {
   const float* lse2;    // [B*H, N_pad]: LSE * log2(e) (-inf kept; padding rows 0)
   const float* delta;   // [B*H, N_pad]: rowsum(dO * O) (padding rows 0)
   __nv_bfloat16* dq;
+  float* dq_acc;        // fused backward only: [B*H, N_pad, 128] fp32 sums of dS K (zeroed before it)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* key_len;  // [B] or nullptr

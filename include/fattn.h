@@ -139,6 +139,13 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
  * it enqueues three kernels (four from head dim 136) on `stream` and returns
  * without synchronising.
  *
+ * With FATTN_BWD_FUSED=1 in the environment (read once per process), head
+ * dims 72..128 run instead a single kernel that also forms dQ, adding each
+ * key tile's share into an fp32 buffer with atomic reductions (another
+ * B*H*ceil(N/128)*128 * 128 * 4 bytes of scratch; two more kernels zero and
+ * convert it).  Its dQ is not bit-reproducible from run to run (the order of
+ * the fp32 additions varies); dK and dV are.
+ *
  * Returns FATTN_OK, FATTN_ERR_INVALID_ARG, FATTN_ERR_UNSUPPORTED (d not a
  * multiple of 8 in [8, 256]) or FATTN_ERR_CUDA, with argument errors detected before anything
  * is enqueued; time-outs of the kernels' bounded waits are reported by

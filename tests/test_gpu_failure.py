@@ -31,13 +31,14 @@ from exact_softmax_attention_fattn_gb300.inputs import Workload, make_inputs
 # each hold one query tile, gets a non-causal problem (every CTA 64 key tiles)
 shapes = {"fwd": (1, 4, 2048, 128, True), "split": (1, 2, 4096, 128, True), "d256": (1, 8, 4096, 256, False),
           "d256split": (1, 2, 4096, 256, False), "bwd256": (1, 2, 1024, 256, True),
-          "bwd": (1, 2, 1024, 128, True), "noalloc": (1, 4, 2048, 128, True), "linear": (2, 4, 4096, 64, True)}
+          "bwd": (1, 2, 1024, 128, True), "bwdfused": (1, 2, 1024, 128, True), "noalloc": (1, 4, 2048, 128, True),
+          "linear": (2, 4, 4096, 64, True)}
 B, H, N, d, causal = shapes[case]
 x = make_inputs(Workload("to", B, H, N, d, causal, 50))
 dev = torch.device("cuda:0")
 q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in (x.q, x.k, x.v))
 o = torch.zeros_like(q); lse = torch.zeros((B, H, N), dtype=torch.float32, device=dev)
-if case in ("bwd", "bwd256"):
+if case in ("bwd", "bwd256", "bwdfused"):
     binding.last_error()                  # start clean
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     binding.backward_into(q, k, v, o, lse, q, dq, dk, dv, causal=causal)
@@ -62,14 +63,17 @@ print(json.dumps({"status": st, "detail": detail, "again": again, "context_ok": 
 """
 
 
-@pytest.mark.parametrize("case", ["fwd", "split", "d256", "d256split", "bwd", "bwd256", "noalloc", "linear"])
+@pytest.mark.parametrize("case", ["fwd", "split", "d256", "d256split", "bwd", "bwd256", "bwdfused", "noalloc", "linear"])
 def test_bounded_wait_times_out_and_reports(cuda_device, case):
     """Each kernel family (the forward, its split-KV instantiation, the
-    256-column forward, the backward's kernels, the tensor-core linear
+    256-column forward, the backward's kernels (and the single-kernel
+    backward), the tensor-core linear
     attention kernels) and the no-alloc entry point (its error word lives
     after its static array) times out for real and reports; the backward runs on zero O and LSE (values do not matter
     here)."""
     env = dict(os.environ, FATTN_WAIT_LIMIT_US="1")
+    if case == "bwdfused":
+        env["FATTN_BWD_FUSED"] = "1"  # the single-kernel backward
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT, case], env=env, capture_output=True, text=True,
                        timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]

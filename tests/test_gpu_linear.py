@@ -24,19 +24,21 @@ pytestmark = pytest.mark.gpu
 GUARD = 4096
 
 
-def run_gpu(x, dev, key_len=None, eps=1e-6):
+def run_gpu(x, dev, key_len=None, eps=1e-6, shift=0):
+    """shift: extra floats before `out` (4 puts it on a 16- but not a 32-byte
+    boundary)."""
     import torch
 
     q, k, v = (torch.from_numpy(a).to(dev) for a in (x.q, x.k, x.v))
     B, H, N, E = q.shape
     M = v.shape[3]
-    buf = torch.full((B * H * N * M + 2 * GUARD,), float("nan"), dtype=torch.float32, device=dev)
-    out = buf[GUARD:GUARD + B * H * N * M].view(B, H, N, M)
+    buf = torch.full((B * H * N * M + 2 * GUARD + shift,), float("nan"), dtype=torch.float32, device=dev)
+    out = buf[GUARD + shift:GUARD + shift + B * H * N * M].view(B, H, N, M)
     binding.linear_forward(q, k, v, key_len=key_len, eps=eps, out=out)
     torch.cuda.synchronize(dev)
     st, detail = binding.last_error()
     assert st == binding.FATTN_OK, detail
-    assert bool(torch.isnan(buf[:GUARD]).all()) and bool(torch.isnan(buf[-GUARD:]).all()), "store outside out"
+    assert bool(torch.isnan(buf[:GUARD + shift]).all()) and bool(torch.isnan(buf[-GUARD:]).all()), "store outside out"
     return out.cpu().numpy().astype(np.float64)
 
 
@@ -64,6 +66,16 @@ def test_linear_key_lengths(cuda_device, E, M):
     ours = run_gpu(x, cuda_device, key_len=kl)
     check(ours, oracle.linear(x.q, x.k, x.v, key_len=kl), x.v, f"key_len E={E} M={M}")
     assert np.all(ours[0] == 0.0)
+
+
+@pytest.mark.parametrize("shift", [4, 8])
+@pytest.mark.parametrize("E,M", [(64, 64), (32, 40), (16, 12)])
+def test_linear_output_alignment(cuda_device, shift, E, M):
+    """Output rows on 16- and 32-byte boundaries, M a multiple of 8 or not:
+    the oracle's result, and nothing stored outside `out`."""
+    x = make_linear_inputs(LinearWorkload("lin_al", 1, 2, 300, E, M, 79 + shift + E + M))
+    check(run_gpu(x, cuda_device, shift=shift), oracle.linear(x.q, x.k, x.v), x.v,
+          f"shift={shift} E={E} M={M}")
 
 
 def test_linear_eps(cuda_device):
