@@ -143,24 +143,17 @@ struct BwdMma {
   static constexpr uint32_t IDESC_KMAJOR = idesc_f16kind(128, 128, true, false);  // both operands K-major
   static constexpr uint32_t IDESC_ACC = idesc_f16kind(128, D, true, true);        // B MN-major, N = D
 
-  // D(128 x 128) = A(128 x D) B(128 x D)^T, both K-major tiles in shared memory.
+  // D(128 x 128) = A(128 x D) B(128 x D)^T, both K-major tiles in shared
+  // memory: D/16 MMAs behind one elect (64-column panels PANEL_BYTES apart).
   __device__ __forceinline__ static void ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
-    static_for<D / 16>([&](auto kc) {
-      constexpr int kk = decltype(kc)::value;
-      constexpr uint32_t off = ((kk / 4) * PANEL_BYTES + (kk % 4) * 32u) >> 4;
-      mma_ss_w_off<off>(d_tmem, a_desc, b_desc, IDESC_KMAJOR, kk > 0 ? 1u : 0u);
-    });
+    mma_ss_batch<D / 16>(d_tmem, a_desc, b_desc, IDESC_KMAJOR, 0u);
   }
   // D(128 x D) (+)= A(128 x 128, bf16 in TMEM) B(128 x D, MN-major tile in shared memory).
   // A is packed by the two elementwise groups into TMEM columns [0, 32) (its
-  // columns 0-63) and [64, 96) (its columns 64-127).
+  // columns 0-63) and [64, 96) (its columns 64-127); eight MMAs of 16 rows
+  // (two 1024-byte row groups of B) behind one elect.
   __device__ __forceinline__ static void ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-    static_for<8>([&](auto kc) {
-      constexpr int kk = decltype(kc)::value;
-      constexpr uint32_t boff = (kk * 2048u) >> 4;            // 16 rows = two 1024-byte row groups
-      constexpr uint32_t acol = 8u * kk + (kk >= 4 ? 32u : 0u);  // 16 columns of packed bf16 = 8 TMEM columns
-      mma_ts_w_off<boff, acol>(d_tmem, a_tmem, b_desc, IDESC_ACC, kk > 0 ? 1u : accumulate);
-    });
+    mma_ts_batch8_halves(d_tmem, a_tmem, b_desc, IDESC_ACC, accumulate);
   }
 };
 
