@@ -208,12 +208,9 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
         const uint64_t kd = k_desc0 + (uint64_t)(((uint32_t)(j % C::SLOTS) * C::KV_BYTES) >> 4);
         const uint32_t dt = tmem + D256_TMEM_S + 64u * (uint32_t)(j & 1);
         tc_fence_after();
-        static_for<D256 / 16>([&](auto kc) {
-          constexpr int k = decltype(kc)::value;
-          constexpr uint32_t aoff = ((k / 4) * C::Q_PANEL + (k % 4) * 32u) >> 4;
-          constexpr uint32_t boff = ((k / 4) * C::KV_PANEL + (k % 4) * 32u) >> 4;
-          mma_ss_w_off2<aoff, boff>(dt, q_desc, kd, IDESC_S, k > 0 ? 1u : 0u);
-        });
+        // 16 MMAs of K = 16 behind one elect (Q panels 16 KB, K panels 8 KB apart)
+        static_assert(D256 == 256 && C::Q_PANEL == 16384u && C::KV_PANEL == 8192u, "panel strides of the batch");
+        mma_ss_batch16_a128_b64(dt, q_desc, kd, IDESC_S, 0u);
         mma_commit_w(bar(C::B_S_FULL + (j & 1)));
         mma_commit_w(bar(C::B_K_EMPTY + j % C::SLOTS));
       };
@@ -243,12 +240,10 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
         // O (+)= P_j V_j: P_j packed over the first 32 columns of its S buffer
         const uint64_t vd = v_desc0 + (uint64_t)(((uint32_t)s * C::KV_BYTES) >> 4);
         const uint32_t at = tmem + D256_TMEM_S + 64u * (uint32_t)(j & 1);
-        static_for<D256_BN / 16>([&](auto kc) {
-          constexpr int k = decltype(kc)::value;
-          constexpr uint32_t boff = (k * 2048u) >> 4;  // 16 keys = two 1024-byte row groups
-          constexpr uint32_t acol = 8u * k;            // 16 keys of P = 8 TMEM columns
-          mma_ts_w_off<boff, acol>(tmem + D256_TMEM_O, at, vd, idesc_pv, (k > 0 || j > 0) ? 1u : 0u);
-        });
+        // 4 MMAs of 16 keys behind one elect (16 keys = 8 TMEM columns of P and
+        // two 1024-byte row groups of V)
+        static_assert(D256_BN == 64, "the P V batch issues 4 MMAs of 16 keys");
+        mma_ts_batch4(tmem + D256_TMEM_O, at, vd, idesc_pv, j > 0 ? 1u : 0u);
         mma_commit_w(bar(C::B_PV_DONE));
         mma_commit_w(bar(C::B_V_EMPTY + s));
         if (j + 2 < n) {

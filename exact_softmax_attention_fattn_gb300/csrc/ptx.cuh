@@ -304,6 +304,76 @@ __device__ __forceinline__ void mma_ts_batch8_halves(uint32_t d_tmem, uint32_t a
       : "memory");
 }
 
+// 16 SS MMAs over K = 256 behind one elect, A and B in 64-column panels of
+// different sizes: A panels 16 KB apart (128-row tiles), B panels 8 KB apart
+// (64-row tiles); descriptors advanced in their low word only.
+__device__ __forceinline__ void mma_ss_batch16_a128_b64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 alo, ahi, blo, bhi, al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 {alo, ahi}, %1;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.u32 al, alo, 2;\n\tadd.u32 bl, blo, 2;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 4;\n\tadd.u32 bl, blo, 4;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 6;\n\tadd.u32 bl, blo, 6;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1024;\n\tadd.u32 bl, blo, 512;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1026;\n\tadd.u32 bl, blo, 514;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1028;\n\tadd.u32 bl, blo, 516;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 1030;\n\tadd.u32 bl, blo, 518;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 2048;\n\tadd.u32 bl, blo, 1024;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 2050;\n\tadd.u32 bl, blo, 1026;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 2052;\n\tadd.u32 bl, blo, 1028;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 2054;\n\tadd.u32 bl, blo, 1030;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 3072;\n\tadd.u32 bl, blo, 1536;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 3074;\n\tadd.u32 bl, blo, 1538;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 3076;\n\tadd.u32 bl, blo, 1540;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "add.u32 al, alo, 3078;\n\tadd.u32 bl, blo, 1542;\n\tmov.b64 ad, {al, ahi};\n\tmov.b64 bd, {bl, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 4 TS MMAs over 64 keys behind one elect: A (P) from tensor memory, 16 keys
+// = 8 columns; B (V, MN-major) 16 rows = 2048 bytes per step.
+__device__ __forceinline__ void mma_ts_batch4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 blo, bhi, bl, at;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 {blo, bhi}, %2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 bl, blo, 128;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 256;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 16;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "add.u32 bl, blo, 384;\n\tmov.b64 bd, {bl, bhi};\n\tadd.u32 at, %1, 24;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, t;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // TS form with the B descriptor advanced by OFF and the A TMEM column by ACOL.
 template <uint32_t OFF, uint32_t ACOL>
 __device__ __forceinline__ void mma_ts_w_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
