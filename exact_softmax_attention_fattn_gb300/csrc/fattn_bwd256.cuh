@@ -19,8 +19,9 @@
 // Every operand moves as 128-column halves (128 rows x 128 columns of bf16,
 // two 128-byte-swizzled panels): the CTA's own tiles stay resident (two
 // halves in the dV pass, four in the others), the streamed tile's pair of
-// halves sits in buffer A and the other streamed operand passes through one
-// half buffer X, half a then half b: 160 KB or 224 KB of shared memory.
+// halves sits in buffer A and the other streamed operand passes through half
+// buffers X: two in the dV pass (both halves of dO in flight at once, 192 KB
+// of shared memory), one in the others (half a then half b, 224 KB).
 // The 256-column products are two N = 128 products, one per output half; the
 // 256-deep contractions S and dP are two K = 128 batches accumulated.
 // Roles as in fattn_bwd.cuh: warps 0-7 elementwise (group g = warp / 4 takes
@@ -42,7 +43,10 @@ struct Bwd256Cfg {
   static constexpr uint32_t RES_OFF = 0;
   static constexpr uint32_t A_OFF = N_RES * HALF;       // the streamed tile's two halves
   static constexpr uint32_t X_OFF = A_OFF + 2u * HALF;  // the other streamed operand, one half at a time
-  static constexpr uint32_t BAR_OFF = X_OFF + HALF;
+  // the dV pass has room for both halves of dO (one buffer each); the others
+  // pass their two halves through one buffer
+  static constexpr int N_X = PASS == BP_DV ? 2 : 1;
+  static constexpr uint32_t BAR_OFF = X_OFF + N_X * HALF;
   static constexpr int B_RES_FULL = 0;
   static constexpr int B_A_FULL = 1;
   static constexpr int B_A_EMPTY = 2;
@@ -53,7 +57,9 @@ struct Bwd256Cfg {
   static constexpr int B_OPS = 7;  // P^T (dV pass) or dS / dS^T stored by the elementwise warps
   static constexpr int B_ACC_FULL = 8;
   static constexpr int B_DRAIN = 9;
-  static constexpr int NUM_BARS = 10;
+  static constexpr int B_X1_FULL = 10;   // dV pass: the second half's buffer
+  static constexpr int B_X1_EMPTY = 11;
+  static constexpr int NUM_BARS = 12;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // tmem base (4 B) + abort flag (4 B)
   // + slack for 1024-byte alignment; at least 120 KB so that one CTA holds an SM
   static constexpr uint32_t SMEM_USED = MISC_OFF + 16 + 1024;
@@ -106,6 +112,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(bar(C::B_A_EMPTY), 1);
     mbar_init(bar(C::B_X_FULL), 1);
     mbar_init(bar(C::B_X_EMPTY), 1);
+    mbar_init(bar(C::B_X1_FULL), 1);
+    mbar_init(bar(C::B_X1_EMPTY), 1);
     mbar_init(bar(C::B_S_FULL), 1);
     mbar_init(bar(C::B_DP_FULL), 1);
     mbar_init(bar(C::B_OPS), 32 * BWD_ELEM_WARPS);
@@ -160,18 +168,29 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int h = 0; h < 2; ++h) load_half(base + C::A_OFF + (uint32_t)h * C::HALF, map_a, h, rs, bar(C::B_A_FULL));
         issued_a = n + 1;
         for (int h = 0; ok && h < 2; ++h) {
-          const int x = 2 * n + h;
-          ok = wait_bar(waiter, bar(C::B_X_EMPTY), (uint32_t)(x & 1) ^ 1u, C::B_X_EMPTY, u);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bar(C::B_X_FULL), C::HALF);
-          load_half(base + C::X_OFF, map_x, h, rs, bar(C::B_X_FULL));
-          issued_x = x + 1;
+          if constexpr (C::N_X == 2) {
+            // half h in buffer h, its phases counted per tile
+            const int full = h ? C::B_X1_FULL : C::B_X_FULL, empty = h ? C::B_X1_EMPTY : C::B_X_EMPTY;
+            ok = wait_bar(waiter, bar(empty), (uint32_t)(n & 1) ^ 1u, empty, u);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(full), C::HALF);
+            load_half(base + C::X_OFF + (uint32_t)h * C::HALF, map_x, h, rs, bar(full));
+            issued_x = n + 1;
+          } else {
+            const int x = 2 * n + h;
+            ok = wait_bar(waiter, bar(C::B_X_EMPTY), (uint32_t)(x & 1) ^ 1u, C::B_X_EMPTY, u);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(C::B_X_FULL), C::HALF);
+            load_half(base + C::X_OFF, map_x, h, rs, bar(C::B_X_FULL));
+            issued_x = x + 1;
+          }
         }
       }
       // drain: copies that may still be in flight after an abort
       drain_wait(bar(C::B_RES_FULL), 0, 20000000ull);
       if (issued_a) drain_wait(bar(C::B_A_FULL), (uint32_t)(issued_a - 1) & 1u, 20000000ull);
       if (issued_x) drain_wait(bar(C::B_X_FULL), (uint32_t)(issued_x - 1) & 1u, 20000000ull);
+      if (C::N_X == 2 && issued_x) drain_wait(bar(C::B_X1_FULL), (uint32_t)(issued_x - 1) & 1u, 20000000ull);
     }
   } else if (count > 0 && warp == BWD_MMA_WARP) {
     // Per streamed tile n: S (two K = 128 batches), then (dK, dQ passes) dP
@@ -219,15 +238,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_after();
       const uint32_t acc = n > 0 ? 1u : 0u;
       if constexpr (PASS == BP_DV) {
-        // dV half h += P^T dO half h (P^T packed over S's columns)
+        // dV half h += P^T dO half h (P^T packed over S's columns; dO half h
+        // in buffer h)
         for (int h = 0; ok && h < 2; ++h) {
-          const int x = 2 * n + h;
-          ok = wait_bar(waiter, bar(C::B_X_FULL), (uint32_t)x & 1u, C::B_X_FULL, u);
+          const int full = h ? C::B_X1_FULL : C::B_X_FULL, empty = h ? C::B_X1_EMPTY : C::B_X_EMPTY;
+          ok = wait_bar(waiter, bar(full), (uint32_t)n & 1u, full, u);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
-          mma_ts_batch8_halves(tmem + BT_ACC0 + 128u * (uint32_t)h, tmem + BT_S, ndesc(C::X_OFF), IDESC_TS, acc);
-          mma_commit_w(bar(C::B_X_EMPTY));
+          mma_ts_batch8_halves(tmem + BT_ACC0 + 128u * (uint32_t)h, tmem + BT_S,
+                               ndesc(C::X_OFF + (uint32_t)h * C::HALF), IDESC_TS, acc);
+          mma_commit_w(bar(empty));
         }
       } else {
         // dK half h += dS^T Q half h, or dQ half h += dS K half h (dS packed
