@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/fattn.h"
@@ -931,6 +932,26 @@ extern "C" FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int
 // fattn_bwd: gradients dQ, dK, dV from dO, the forward's O and LSE.
 namespace {
 
+// Launches `kernel` as a programmatic dependent of the kernel before it on
+// `stream`: its CTAs may start (set-up, loads of inputs the caller owns) as
+// the earlier grid's CTAs retire; each reads what that grid wrote only after
+// griddepcontrol.wait, and every CTA of it waits there before it exits.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int D>
 int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                 fattn::BwdParams p, float* rows, cudaStream_t stream) {
@@ -958,14 +979,20 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
       encode_map(&mdo, dout, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
     return FATTN_ERR_CUDA;
   const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
+  // The two kernels read only the call's inputs and the prep kernel's rows,
+  // so each starts as a programmatic dependent of the one before it.
   mark_kernel_start(stream);
-  fattn::fattn_bwd_dkdv_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo,
-                                                                                                      p);
+  cudaError_t e = launch_dependent(fattn::fattn_bwd_dkdv_kernel<D>, grid, fattn::BWD_THREADS,
+                                   fattn::BwdCfg<D>::SMEM_BYTES, stream, mq, mk, mv, mdo, p);
   mark_kernel_stop(stream);
-  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  fattn::fattn_bwd_dq_kernel<D><<<grid, fattn::BWD_THREADS, fattn::BwdDqCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv,
-                                                                                                      mdo, p);
-  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  if (e == cudaSuccess)
+    e = launch_dependent(fattn::fattn_bwd_dq_kernel<D>, grid, fattn::BWD_THREADS, fattn::BwdDqCfg<D>::SMEM_BYTES,
+                         stream, mq, mk, mv, mdo, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  return FATTN_OK;
 }
 
 // Head dims 72..128 in one pass (fattn_bwd_fused.cuh): the prep kernel, the
@@ -1045,17 +1072,24 @@ int enqueue_bwd256(const void* q, const void* k, const void* v, const void* o, c
       encode_map(&mdo, dout, BH, p.N, p.hd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != FATTN_OK)
     return FATTN_ERR_CUDA;
   const unsigned grid = (unsigned)((long long)BH * p.n_tiles);
-  fattn::fattn_bwd256_kernel<fattn::BP_DV>
-      <<<grid, fattn::BWD_THREADS, fattn::Bwd256Cfg<fattn::BP_DV>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
-  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  mark_kernel_start(stream);
-  fattn::fattn_bwd256_kernel<fattn::BP_DK>
-      <<<grid, fattn::BWD_THREADS, fattn::Bwd256Cfg<fattn::BP_DK>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
-  mark_kernel_stop(stream);
-  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
-  fattn::fattn_bwd256_kernel<fattn::BP_DQ>
-      <<<grid, fattn::BWD_THREADS, fattn::Bwd256Cfg<fattn::BP_DQ>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
-  return cudaGetLastError() == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  // The passes read only the call's inputs and the prep kernel's rows, so
+  // each starts as a programmatic dependent of the one before it.
+  cudaError_t e = launch_dependent(fattn::fattn_bwd256_kernel<fattn::BP_DV>, grid, fattn::BWD_THREADS,
+                                   fattn::Bwd256Cfg<fattn::BP_DV>::SMEM_BYTES, stream, mq, mk, mv, mdo, p);
+  if (e == cudaSuccess) {
+    mark_kernel_start(stream);
+    e = launch_dependent(fattn::fattn_bwd256_kernel<fattn::BP_DK>, grid, fattn::BWD_THREADS,
+                         fattn::Bwd256Cfg<fattn::BP_DK>::SMEM_BYTES, stream, mq, mk, mv, mdo, p);
+    mark_kernel_stop(stream);
+  }
+  if (e == cudaSuccess)
+    e = launch_dependent(fattn::fattn_bwd256_kernel<fattn::BP_DQ>, grid, fattn::BWD_THREADS,
+                         fattn::Bwd256Cfg<fattn::BP_DQ>::SMEM_BYTES, stream, mq, mk, mv, mdo, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  return FATTN_OK;
 }
 
 }  // namespace

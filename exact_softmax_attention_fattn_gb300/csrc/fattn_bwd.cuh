@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(PREP_THREADS)
     fattn_bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout, const float* __restrict__ lse,
                           float* __restrict__ lse2, float* __restrict__ delta, int N, int N_pad, int hd_arg,
                           long long n_rows) {
+  pdl_launch_dependents();  // the next kernel may start its set-up now (it waits before reading LSE2 and D)
   const int hd = FULL ? D : hd_arg;
   constexpr int TPR = D / 8;  // threads per row
   const long long r = ((long long)blockIdx.x * PREP_THREADS + threadIdx.x) / TPR;
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t tmem = *tmem_base_slot;
   Waiter waiter{abort_flag, p.err, p.wait_limit_ns, 0};
   const int u = (int)blockIdx.x;
+  pdl_launch_dependents();
 
   if (n_q > 0 && warp == BWD_PRODUCER_WARP) {
     if (lane == 0) {
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tma_load_3d(base + C::FIX0_OFF + pn * PANEL_BYTES, &tmap_k, bar(C::B_FIX_FULL), 64 * pn, key0, bh);
         tma_load_3d(base + C::FIX1_OFF + pn * PANEL_BYTES, &tmap_v, bar(C::B_FIX_FULL), 64 * pn, key0, bh);
       }
+      pdl_wait();  // LSE2 and D come from the prep kernel
       int issued = 0;
       for (int n = 0; ok && n < n_q; ++n) {
         const int s = n % BWD_STAGES;
@@ -359,6 +362,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
     }
   } else if (warp < BWD_ELEM_WARPS) {
+    // every CTA waits here, even one with no query tile, so that this grid
+    // ends after the kernels it depends on
+    pdl_wait();
     waiter.role = ROLE_SOFTMAX;
     const int g = warp / 4;             // column group: tile columns [64g, 64g + 64)
     const int quarter = warp % 4;       // TMEM lane quarter
@@ -674,6 +680,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
     }
   } else if (warp < BWD_ELEM_WARPS) {
+    pdl_wait();  // LSE2 and D come from the prep kernel (every CTA waits, as above)
     waiter.role = ROLE_SOFTMAX;
     const int g = warp / 4;             // column group: tile columns (keys) [64g, 64g + 64)
     const int quarter = warp % 4;       // TMEM lane quarter

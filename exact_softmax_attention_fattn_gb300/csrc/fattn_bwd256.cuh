@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
   Waiter waiter{abort_flag, p.err, p.wait_limit_ns, 0};
+  pdl_launch_dependents();
 
   if (count > 0 && warp == BWD_PRODUCER_WARP) {
     if (lane == 0) {
@@ -265,6 +266,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       drain_wait(bar(C::B_DRAIN), 0, 50000000ull);
     }
   } else if (warp < BWD_ELEM_WARPS) {
+    // LSE2 and D come from the prep kernel; only these warps read them, and
+    // every CTA waits here so that this grid ends after the ones before it
+    pdl_wait();
     waiter.role = ROLE_SOFTMAX;
     const int g = warp / 4;             // column group: tile columns [64g, 64g + 64)
     const int quarter = warp % 4;       // TMEM lane quarter

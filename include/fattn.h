@@ -133,7 +133,9 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o, fl
  *
  * A query row with no visible key gets dQ = 0; a key visible to no query
  * (key_len) gets dK = dV = 0.  All device pointers 16-byte aligned (lse and
- * key_len 4-byte); the caller owns every tensor.  Each call takes
+ * key_len 4-byte); dq, dk and dv overlap neither each other nor any input
+ * (the kernels after the first start before it ends); the caller owns every
+ * tensor.  Each call takes
  * 2 * B*H*ceil(N/128)*128 * 4 bytes of scratch from the library's pool on
  * `stream` (per-row D and LSE in base 2) and returns it in stream order;
  * it enqueues three kernels (four from head dim 136) on `stream` and returns
