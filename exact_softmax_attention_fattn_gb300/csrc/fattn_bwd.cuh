@@ -659,15 +659,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // dQ += dS_n K_n (dS over the first 64 columns of S buffer n % 2); K_n is then free
-      M::ts(tmem + BQ_DQ, tmem + BQ_S0 + 128u * (uint32_t)(n & 1), smem_desc(k_addr(n), PANEL_BYTES, 1024),
-            n > 0 ? 1u : 0u);
-      mma_commit_w(bar(C::B_K_EMPTY + n % C::K_SLOTS));
+      // dP_n+1 first: the elementwise warps have read dP_n, and the next
+      // tile's dS waits on nothing else (its exponentials run meanwhile)
       if (n + 1 < n_k) {
         wait_v(n + 1);
         if (!ok) break;
         issue_dp(n + 1);
       }
+      // dQ += dS_n K_n (dS over the first 64 columns of S buffer n % 2); K_n is then free
+      M::ts(tmem + BQ_DQ, tmem + BQ_S0 + 128u * (uint32_t)(n & 1), smem_desc(k_addr(n), PANEL_BYTES, 1024),
+            n > 0 ? 1u : 0u);
+      mma_commit_w(bar(C::B_K_EMPTY + n % C::K_SLOTS));
       if (n + 2 < n_k) {
         wait_k(n + 2);
         if (!ok) break;
