@@ -26,6 +26,27 @@
 
 namespace {
 
+// Launches `kernel` as a programmatic dependent of the kernel before it on
+// `stream`: its CTAs may start (set-up, loads of inputs the caller owns) as
+// the earlier grid's CTAs retire; each reads what that grid wrote only after
+// griddepcontrol.wait, and every CTA of it waits there before it exits.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, unsigned block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+
 constexpr int kMaxDevices = 64;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -495,10 +516,15 @@ int enqueue(const void* q, const void* k, const void* v, fattn::Params p, void* 
   if (p.n_splits > 1) {
     constexpr int rows_per_block = fattn::COMBINE_THREADS / (D / 16);
     const dim3 cgrid((unsigned)((p.N + rows_per_block - 1) / rows_per_block), (unsigned)(BH < 65535 ? BH : 65535));
-    fattn::fattn_splitkv_combine_kernel<D><<<cgrid, fattn::COMBINE_THREADS, 0, stream>>>(
-        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.hd, p.causal, p.n_splits,
-        fattn::QT * fattn::BM, fattn::BN);
-    if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+    // a programmatic dependent of the attention kernel: its launch overlaps
+    // the attention kernel's last CTAs, and it reads the partials only after
+    // griddepcontrol.wait
+    if (launch_dependent(fattn::fattn_splitkv_combine_kernel<D>, cgrid, fattn::COMBINE_THREADS, 0, stream,
+                         (const float*)p.o_part, (const float*)p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N,
+                         p.hd, p.causal, p.n_splits, fattn::QT * fattn::BM, fattn::BN) != cudaSuccess) {
+      cudaGetLastError();
+      return FATTN_ERR_CUDA;
+    }
   }
   return FATTN_OK;
 }
@@ -555,10 +581,12 @@ int enqueue_d256(const void* q, const void* k, const void* v, fattn::Params p, v
   if (split) {
     constexpr int rows_per_block = fattn::COMBINE_THREADS / (fattn::D256 / 16);
     const dim3 cgrid((unsigned)((p.N + rows_per_block - 1) / rows_per_block), (unsigned)(BH < 65535 ? BH : 65535));
-    fattn::fattn_splitkv_combine_kernel<fattn::D256><<<cgrid, fattn::COMBINE_THREADS, 0, stream>>>(
-        p.o_part, p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N, p.hd, p.causal, p.n_splits, fattn::BM,
-        fattn::D256_BN);
-    if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
+    if (launch_dependent(fattn::fattn_splitkv_combine_kernel<fattn::D256>, cgrid, fattn::COMBINE_THREADS, 0, stream,
+                         (const float*)p.o_part, (const float*)p.lse_part, p.o, p.lse, p.key_len, p.B, p.H, p.N,
+                         p.hd, p.causal, p.n_splits, fattn::BM, fattn::D256_BN) != cudaSuccess) {
+      cudaGetLastError();
+      return FATTN_ERR_CUDA;
+    }
   }
   return FATTN_OK;
 }
@@ -931,26 +959,6 @@ extern "C" FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int
 // ------------------------------------------------------------------------
 // fattn_bwd: gradients dQ, dK, dV from dO, the forward's O and LSE.
 namespace {
-
-// Launches `kernel` as a programmatic dependent of the kernel before it on
-// `stream`: its CTAs may start (set-up, loads of inputs the caller owns) as
-// the earlier grid's CTAs retire; each reads what that grid wrote only after
-// griddepcontrol.wait, and every CTA of it waits there before it exits.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                             cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
 
 template <int D>
 int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

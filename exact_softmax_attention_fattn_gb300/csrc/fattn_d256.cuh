@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(D256_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
+  if constexpr (SPLIT) pdl_launch_dependents();  // the combine kernel may launch now (it waits before reading)
   Waiter waiter{abort_flag, p.err, p.wait_limit_ns, 0};
 
   if (warp == D256_PRODUCER_WARP) {

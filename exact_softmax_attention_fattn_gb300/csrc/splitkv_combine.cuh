@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace fattn {
 
 constexpr int COMBINE_THREADS = 256;
@@ -53,6 +55,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS)
   const int row = blockIdx.x * ROWS + threadIdx.x / TPR;  // grid: (row blocks, heads)
   const int c4 = threadIdx.x % TPR;                       // float4 columns c4 + TPR * i, i < VPT
   if (row >= N) return;
+  pdl_wait();  // the partials come from the attention kernel before this one
   const int BH = B * H;
   const size_t stride = (size_t)BH * N;  // rows between two splits' partials
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
