@@ -447,12 +447,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
             const float4 d4 = del4[q4];
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float dsv[4];
+            // dS = P (dP - D) on pairs of columns (f32x2: the same two
+            // roundings as the scalar form, half the instructions)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dsv[e] = pr[4 * q4 + e] * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
-            dk2[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-            dk2[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+            for (int h = 0; h < 2; ++h) {
+              const int q = 4 * q4 + 2 * h;
+              const uint64_t dd = h ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+              const uint64_t ds = f2_mul(f2_pack(pr[q], pr[q + 1]),
+                                         f2_sub(f2_pack(__uint_as_float(dh[q]), __uint_as_float(dh[q + 1])), dd));
+              float lo, hi;
+              f2_unpack(ds, lo, hi);
+              dk2[2 * q4 + h] = pack_bf16x2(lo, hi);
+            }
           }
           tmem_st32(dp_addr, dk2);
         }
@@ -719,13 +725,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld_wait(sh);
           // a separate copy of the loop for masked tiles (no per-element
           // selects on the others)
+          // exponent arguments S c - LSE2 two columns per f32x2 FMA
+          const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2);
           auto p_loop = [&](auto masked_c) {
             constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
-            for (int q = 0; q < 64; ++q) {
-              float pe = ex2(fmaf(__uint_as_float(sh[q]), c, -lse2));
-              if constexpr (MASKED) pe = q < vis_n ? pe : 0.0f;
-              pr[q] = pe;
+            for (int q = 0; q < 64; q += 2) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[q]), __uint_as_float(sh[q + 1])), c2, nl2), x0, x1);
+              float p0 = ex2(x0), p1 = ex2(x1);
+              if constexpr (MASKED) {
+                p0 = q < vis_n ? p0 : 0.0f;
+                p1 = q + 1 < vis_n ? p1 : 0.0f;
+              }
+              pr[q] = p0;
+              pr[q + 1] = p1;
             }
           };
           if (masked)
@@ -743,10 +757,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld64(dp_addr, dh);
           tmem_ld_wait(dh);
           uint32_t pk[32];
+          const uint64_t d2 = f2_pack(drow, drow);
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            pk[q] = pack_bf16x2(pr[2 * q] * (__uint_as_float(dh[2 * q]) - drow),
-                                pr[2 * q + 1] * (__uint_as_float(dh[2 * q + 1]) - drow));
+          for (int q = 0; q < 32; ++q) {
+            // dS = P (dP - D), two columns per f32x2 op
+            const uint64_t ds = f2_mul(f2_pack(pr[2 * q], pr[2 * q + 1]),
+                                       f2_sub(f2_pack(__uint_as_float(dh[2 * q]), __uint_as_float(dh[2 * q + 1])), d2));
+            float lo, hi;
+            f2_unpack(ds, lo, hi);
+            pk[q] = pack_bf16x2(lo, hi);
+          }
           tmem_st32(s_addr, pk);
         }
         tmem_st_wait();
