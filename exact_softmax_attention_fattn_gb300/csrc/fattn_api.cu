@@ -965,19 +965,19 @@ int enqueue_bwd(const void* q, const void* k, const void* v, const void* o, cons
                 fattn::BwdParams p, float* rows, cudaStream_t stream) {
   const int BH = p.B * p.H;
   const long long n_rows = (long long)BH * p.N_pad;
-  float* lse2 = rows;
+  float* nlse2 = rows;
   float* delta = rows + n_rows;
-  p.lse2 = lse2;
+  p.nlse2 = nlse2;
   p.delta = delta;
   const long long prep_threads = n_rows * (D / 8);
   const unsigned prep_blocks = (unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS);
   if (p.hd == D)
     fattn::fattn_bwd_prep_kernel<D, true><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, nlse2, delta, p.N, p.N_pad, p.hd,
         n_rows);
   else
     fattn::fattn_bwd_prep_kernel<D, false><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, nlse2, delta, p.N, p.N_pad, p.hd,
         n_rows);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo;
@@ -1011,7 +1011,7 @@ int enqueue_bwd_fused(const void* q, const void* k, const void* v, const void* o
   constexpr int D = fattn::FB_D;
   const int BH = p.B * p.H;
   const long long n_rows = (long long)BH * p.N_pad;
-  p.lse2 = rows;
+  p.nlse2 = rows;
   p.delta = rows + n_rows;
   p.dq_acc = dq_acc;
   const long long prep_threads = n_rows * (D / 8);
@@ -1057,20 +1057,20 @@ int enqueue_bwd256(const void* q, const void* k, const void* v, const void* o, c
                    fattn::BwdParams p, float* rows, cudaStream_t stream) {
   const int BH = p.B * p.H;
   const long long n_rows = (long long)BH * p.N_pad;
-  float* lse2 = rows;
+  float* nlse2 = rows;
   float* delta = rows + n_rows;
-  p.lse2 = lse2;
+  p.nlse2 = nlse2;
   p.delta = delta;
   constexpr int D = fattn::D256;
   const long long prep_threads = n_rows * (D / 8);
   const unsigned prep_blocks = (unsigned)((prep_threads + fattn::PREP_THREADS - 1) / fattn::PREP_THREADS);
   if (p.hd == D)
     fattn::fattn_bwd_prep_kernel<D, true><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, nlse2, delta, p.N, p.N_pad, p.hd,
         n_rows);
   else
     fattn::fattn_bwd_prep_kernel<D, false><<<prep_blocks, fattn::PREP_THREADS, 0, stream>>>(
-        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, lse2, delta, p.N, p.N_pad, p.hd,
+        reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dout), lse, nlse2, delta, p.N, p.N_pad, p.hd,
         n_rows);
   if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo;
@@ -1140,7 +1140,7 @@ extern "C" FATTN_API int fattn_bwd(const void* q, const void* k, const void* v, 
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.causal = causal ? 1 : 0;
   p.wait_limit_ns = wait_limit_ns();
-  p.lse2 = nullptr;
+  p.nlse2 = nullptr;
   p.delta = nullptr;
   p.dq_acc = nullptr;
   if ((long long)B * H * p.n_tiles > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;

@@ -10,7 +10,7 @@
 // O_i = sum_k P_ik V_k.
 //
 // How (GB300):
-//   * fattn_bwd_prep_kernel: D per row and LSE * log2(e), both written to
+//   * fattn_bwd_prep_kernel: D per row and -LSE * log2(e), both written to
 //     buffers whose rows are padded to a multiple of 128, so every per-tile
 //     copy of them is a 512-byte, 16-byte-aligned bulk copy for any N.
 //   * fattn_bwd_dkdv_kernel: one CTA per (batch*head, 128-key tile j).  K_j
@@ -49,7 +49,7 @@ constexpr int BWD_STAGES = 2;
 constexpr int PREP_THREADS = 256;
 
 struct BwdParams {
-  const float* lse2;    // [B*H, N_pad]: LSE * log2(e) (-inf kept; padding rows 0)
+  const float* nlse2;   // [B*H, N_pad]: -LSE * log2(e) (+inf for an empty row; padding rows 0)
   const float* delta;   // [B*H, N_pad]: rowsum(dO * O) (padding rows 0)
   __nv_bfloat16* dq;
   float* dq_acc;        // fused backward only: [B*H, N_pad, 128] fp32 sums of dS K (zeroed before it)
@@ -68,12 +68,12 @@ struct BwdParams {
 
 // ------------------------------------------------------------------ prep
 // One row per D/8 threads (16-byte loads of O and dO; a row has hd <= D
-// elements); rows past N (padding) get D = 0 and LSE2 = 0.
+// elements); rows past N (padding) get D = 0 and -LSE2 = 0.
 // FULL: hd == D, the row length a compile-time constant.
 template <int D, bool FULL>
 __global__ void __launch_bounds__(PREP_THREADS)
     fattn_bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout, const float* __restrict__ lse,
-                          float* __restrict__ lse2, float* __restrict__ delta, int N, int N_pad, int hd_arg,
+                          float* __restrict__ nlse2, float* __restrict__ delta, int N, int N_pad, int hd_arg,
                           long long n_rows) {
   pdl_launch_dependents();  // the next kernel may start its set-up now (it waits before reading LSE2 and D)
   const int hd = FULL ? D : hd_arg;
@@ -98,13 +98,13 @@ __global__ void __launch_bounds__(PREP_THREADS)
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (r < n_rows && part == 0) {
     delta[r] = live ? acc : 0.0f;
-    lse2[r] = live ? lse[(size_t)bh * (size_t)N + (size_t)i] * 1.4426950408889634f : 0.0f;
+    nlse2[r] = live ? lse[(size_t)bh * (size_t)N + (size_t)i] * -1.4426950408889634f : 0.0f;
   }
 }
 
 // ------------------------------------------------------------------ shared layout
 // Both main kernels: two stationary 128-row tiles, a BWD_STAGES ring of two
-// tiles each, and (dK/dV kernel) 512 bytes of LSE2 + 512 of D per stage.
+// tiles each, and (dK/dV kernel) 512 bytes of -LSE2 + 512 of D per stage.
 template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head-dim bucket 64 or 128");
@@ -114,7 +114,7 @@ struct BwdCfg {
   static constexpr uint32_t FIX1_OFF = TILE_BYTES;       // V_j (dK/dV) or dO_i (dQ)
   static constexpr uint32_t RING_OFF = 2 * TILE_BYTES;   // per stage: two tiles
   static constexpr uint32_t STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr uint32_t ROWS_OFF = RING_OFF + BWD_STAGES * STAGE_BYTES;  // per stage: LSE2[128], D[128]
+  static constexpr uint32_t ROWS_OFF = RING_OFF + BWD_STAGES * STAGE_BYTES;  // per stage: -LSE2[128], D[128]
   static constexpr uint32_t BAR_OFF = ROWS_OFF + BWD_STAGES * 1024u;
   // barrier ids
   static constexpr int B_FIX_FULL = 0;
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tma_load_3d(st + C::TILE_BYTES + pn * PANEL_BYTES, &tmap_do, full, 64 * pn, q0, bh);
         }
         const size_t row = (size_t)bh * (size_t)p.N_pad + (size_t)q0;
-        bulk_load(base + C::ROWS_OFF + (uint32_t)s * 1024u, p.lse2 + row, 512u, full);
+        bulk_load(base + C::ROWS_OFF + (uint32_t)s * 1024u, p.nlse2 + row, 512u, full);
         bulk_load(base + C::ROWS_OFF + (uint32_t)s * 1024u + 512u, p.delta + row, 512u, full);
         issued = n + 1;
       }
@@ -392,8 +392,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float4* lse4 = reinterpret_cast<const float4*>(base_ptr + C::ROWS_OFF + (uint32_t)s * 1024u) + 16 * g;
-        const float4* del4 = lse4 + 32;
+        const float4* nlse4 = reinterpret_cast<const float4*>(base_ptr + C::ROWS_OFF + (uint32_t)s * 1024u) + 16 * g;
+        const float4* del4 = nlse4 + 32;
+        const uint64_t c2 = f2_pack(c, c);
         // visible columns: query q0 + col sees this key iff the key is inside
         // key_len and (causal) key <= query; rows past N read as zero and
         // contribute nothing (their dO and Q are zero)
@@ -412,12 +413,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
-              const float4 l4 = lse4[q4];
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              // exponent arguments S c - LSE2, two columns per f32x2 FMA
+              const float4 l4 = nlse4[q4];
+              float x[4];
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[4 * q4]), __uint_as_float(sh[4 * q4 + 1])), c2,
+                               f2_pack(l4.x, l4.y)),
+                        x[0], x[1]);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[4 * q4 + 2]), __uint_as_float(sh[4 * q4 + 3])), c2,
+                               f2_pack(l4.z, l4.w)),
+                        x[2], x[3]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int col = 64 * g + 4 * q4 + e;
-                float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
+                float pe = ex2(x[e]);
                 if constexpr (MASKED) pe = (key_vis && col >= min_q) ? pe : 0.0f;
                 pr[4 * q4 + e] = pe;
               }
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint32_t dp_addr = tmem + lane_off + BQ_DP + 64u * (uint32_t)g;
       const float c = p.scale_log2;
       const size_t prow = (size_t)bh * (size_t)p.N_pad + (size_t)query;
-      const float lse2 = p.lse2[prow];
+      const float nlse2 = p.nlse2[prow];
       const float drow = p.delta[prow];
       // keys [0, lim) are visible to this row
       const int lim = p.causal ? min(kl, query + 1) : kl;
@@ -726,7 +734,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           // a separate copy of the loop for masked tiles (no per-element
           // selects on the others)
           // exponent arguments S c - LSE2 two columns per f32x2 FMA
-          const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2);
+          const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(nlse2, nlse2);
           auto p_loop = [&](auto masked_c) {
             constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll

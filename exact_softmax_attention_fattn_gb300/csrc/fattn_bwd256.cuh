@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const size_t rows_bh = (size_t)bh * (size_t)p.N_pad;
       // dQ pass: LSE and D are constants of the lane's query row (rows past N
       // are padding, 0)
-      const float lse2_row = KEYS ? 0.0f : __ldg(p.lse2 + rows_bh + own);
+      const float nlse2_row = KEYS ? 0.0f : __ldg(p.nlse2 + rows_bh + own);
       const float delta_row = KEYS ? 0.0f : __ldg(p.delta + rows_bh + own);
       bool ok = true;
       for (int n = 0; ok && n < count; ++n) {
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           end_vis = min(64, max(0, (p.causal ? min(kl, own + 1) : kl) - c0));
         }
         const bool any_mask = first_vis > 0 || end_vis < 64;
-        const float4* lse4 = reinterpret_cast<const float4*>(p.lse2 + rows_bh + c0);
+        const float4* nlse4 = reinterpret_cast<const float4*>(p.nlse2 + rows_bh + c0);
         float pr[64];
         {
           uint32_t sh[64];
@@ -325,17 +325,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
-              float lv[4];
+              // exponent arguments S c - LSE2, two per f32x2 FMA: -LSE2 per
+              // column (dV, dK passes) or per row (dQ pass)
+              const uint64_t c2 = f2_pack(c, c);
+              uint64_t nl[2];
               if constexpr (KEYS) {
-                const float4 l4 = __ldg(lse4 + q4);
-                lv[0] = l4.x, lv[1] = l4.y, lv[2] = l4.z, lv[3] = l4.w;
+                const float4 l4 = __ldg(nlse4 + q4);
+                nl[0] = f2_pack(l4.x, l4.y);
+                nl[1] = f2_pack(l4.z, l4.w);
               } else {
-                lv[0] = lv[1] = lv[2] = lv[3] = lse2_row;
+                nl[0] = nl[1] = f2_pack(nlse2_row, nlse2_row);
+              }
+              float x[4];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int i = 4 * q4 + 2 * h;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[i]), __uint_as_float(sh[i + 1])), c2, nl[h]), x[2 * h],
+                          x[2 * h + 1]);
               }
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int i = 4 * q4 + e;
-                float pe = ex2(fmaf(__uint_as_float(sh[i]), c, -lv[e]));
+                float pe = ex2(x[e]);
                 if constexpr (MASKED) pe = (i >= first_vis && i < end_vis) ? pe : 0.0f;
                 pr[i] = pe;
               }
@@ -371,11 +382,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             } else {
               dv[0] = dv[1] = dv[2] = dv[3] = delta_row;
             }
-            float ds[4];
+            // two columns per f32x2 op (the same roundings as the scalar form)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) ds[e] = pr[4 * q4 + e] * (__uint_as_float(dh[4 * q4 + e]) - dv[e]);
-            pk[2 * q4] = pack_bf16x2(ds[0], ds[1]);
-            pk[2 * q4 + 1] = pack_bf16x2(ds[2], ds[3]);
+            for (int h = 0; h < 2; ++h) {
+              const int i = 4 * q4 + 2 * h;
+              const uint64_t ds = f2_mul(f2_pack(pr[i], pr[i + 1]),
+                                         f2_sub(f2_pack(__uint_as_float(dh[i]), __uint_as_float(dh[i + 1])),
+                                                f2_pack(dv[2 * h], dv[2 * h + 1])));
+              float lo, hi;
+              f2_unpack(ds, lo, hi);
+              pk[2 * q4 + h] = pack_bf16x2(lo, hi);
+            }
           }
           tmem_st32(dp_addr, pk);
         }

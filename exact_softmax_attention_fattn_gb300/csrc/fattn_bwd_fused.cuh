@@ -72,7 +72,7 @@ struct FusedCfg {
   static constexpr uint32_t STAGE_BYTES = 2 * Q_TILE;
   static constexpr uint32_t DS_OFF = RING_OFF + FB_STAGES * STAGE_BYTES;  // [2] dS^T tiles
   static constexpr uint32_t DS_BYTES = 128u * FB_BQ * 2u;   // 128 keys x 64 queries bf16
-  static constexpr uint32_t ROWS_OFF = DS_OFF + 2 * DS_BYTES;             // per stage: LSE2[64], D[64]
+  static constexpr uint32_t ROWS_OFF = DS_OFF + 2 * DS_BYTES;             // per stage: -LSE2[64], D[64]
   static constexpr uint32_t ROWS_BYTES = 2u * FB_BQ * 4u;
   static constexpr uint32_t BAR_OFF = ROWS_OFF + FB_STAGES * ROWS_BYTES;
   // barrier ids
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
         }
         const size_t row = (size_t)bh * (size_t)p.N_pad + (size_t)q0;
         const uint32_t rows = base + C::ROWS_OFF + (uint32_t)s * C::ROWS_BYTES;
-        bulk_load(rows, p.lse2 + row, FB_BQ * 4u, full);
+        bulk_load(rows, p.nlse2 + row, FB_BQ * 4u, full);
         bulk_load(rows + FB_BQ * 4u, p.delta + row, FB_BQ * 4u, full);
         issued = n + 1;
       }
@@ -411,9 +411,9 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float4* lse4 =
+        const float4* nlse4 =
             reinterpret_cast<const float4*>(base_ptr + C::ROWS_OFF + (uint32_t)s * C::ROWS_BYTES) + (FB_CW / 4) * g;
-        const float4* del4 = lse4 + FB_BQ / 4;
+        const float4* del4 = nlse4 + FB_BQ / 4;
         // visible columns: query q0 + col sees this key iff the key is inside
         // key_len and (causal) key <= query; rows past N read as zero and
         // contribute nothing (their dO and Q are zero)
@@ -430,12 +430,20 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
             constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
             for (int q4 = 0; q4 < FB_CW / 4; ++q4) {
-              const float4 l4 = lse4[q4];
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              // exponent arguments S c - LSE2 (-LSE2 per column), two per f32x2 FMA
+              const float4 l4 = nlse4[q4];
+              const uint64_t c2 = f2_pack(c, c);
+              float x[4];
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[4 * q4]), __uint_as_float(sh[4 * q4 + 1])), c2,
+                               f2_pack(l4.x, l4.y)),
+                        x[0], x[1]);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sh[4 * q4 + 2]), __uint_as_float(sh[4 * q4 + 3])), c2,
+                               f2_pack(l4.z, l4.w)),
+                        x[2], x[3]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int col = FB_CW * g + 4 * q4 + e;
-                float pe = ex2(fmaf(__uint_as_float(sh[4 * q4 + e]), c, -lv[e]));
+                float pe = ex2(x[e]);
                 if constexpr (MASKED) pe = (key_vis && col >= min_q) ? pe : 0.0f;
                 pr[4 * q4 + e] = pe;
               }
@@ -466,12 +474,17 @@ __global__ void __launch_bounds__(FB_THREADS, 1)
 #pragma unroll
           for (int q4 = 0; q4 < FB_CW / 4; ++q4) {
             const float4 d4 = del4[q4];
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float dsv[4];
+            // two columns per f32x2 op (the same roundings as the scalar form)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dsv[e] = pr[4 * q4 + e] * (__uint_as_float(dh[4 * q4 + e]) - dv4[e]);
-            dk2[2 * q4] = pack_bf16x2(dsv[0], dsv[1]);
-            dk2[2 * q4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+            for (int h = 0; h < 2; ++h) {
+              const int i = 4 * q4 + 2 * h;
+              const uint64_t dd = h ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+              const uint64_t ds = f2_mul(f2_pack(pr[i], pr[i + 1]),
+                                         f2_sub(f2_pack(__uint_as_float(dh[i]), __uint_as_float(dh[i + 1])), dd));
+              float lo, hi;
+              f2_unpack(ds, lo, hi);
+              dk2[2 * q4 + h] = pack_bf16x2(lo, hi);
+            }
           }
           tmem_st8(dp_addr, dk2);
           uint8_t* ds_tile = base_ptr + C::DS_OFF + (uint32_t)(n & 1) * C::DS_BYTES + ds_row;
