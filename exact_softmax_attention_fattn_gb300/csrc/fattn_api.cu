@@ -60,6 +60,12 @@ struct DeviceState {
   cudaMemPool_t pool = nullptr;   // private stream-ordered pool for per-call scratch
   cudaStream_t copy_in = nullptr;   // host-buffer entry point: host -> device copies
   cudaStream_t copy_out = nullptr;  // and device -> host copies
+  // The host-buffer entry point's events, made once and reused from call to
+  // call (a wait enqueued on an event refers to the record before it, so a
+  // later call may record the event again); its calls on one device enqueue
+  // one at a time under host_mu.
+  std::mutex host_mu;
+  std::vector<cudaEvent_t> host_events;
 };
 
 std::mutex g_mu;
@@ -769,10 +775,17 @@ extern "C" FATTN_API int fattn_fwd_host(const void* q, const void* k, const void
 
   const std::vector<HostChunk> chunks = host_chunks(B, H, (long long)(n_elem * 2u));
   const int nc = (int)chunks.size();
-  std::vector<cudaEvent_t> ev(2 * nc + 2, nullptr);
-  for (auto& e : ev)
-    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) rc = FATTN_ERR_CUDA;
-  cudaEvent_t ev_alloc = ev[2 * nc], ev_done = ev[2 * nc + 1];
+  std::lock_guard<std::mutex> host_lock(ds->host_mu);
+  while ((int)ds->host_events.size() < 2 * nc + 2) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      rc = FATTN_ERR_CUDA;
+      break;
+    }
+    ds->host_events.push_back(e);
+  }
+  const std::vector<cudaEvent_t>& ev = ds->host_events;
+  cudaEvent_t ev_alloc = rc == FATTN_OK ? ev[2 * nc] : nullptr, ev_done = rc == FATTN_OK ? ev[2 * nc + 1] : nullptr;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
   if (rc == FATTN_OK && !(ok(cudaEventRecord(ev_alloc, s)) && ok(cudaStreamWaitEvent(ds->copy_in, ev_alloc, 0))))
     rc = FATTN_ERR_CUDA;
@@ -811,9 +824,10 @@ extern "C" FATTN_API int fattn_fwd_host(const void* q, const void* k, const void
       rc = FATTN_ERR_CUDA;
   }
   // join both copy streams back into the caller's stream, then release the buffers there
-  cudaEvent_t ev_in_done = ev[2 * nc];  // reused: the allocation event has been consumed
-  bool joined = ok(cudaEventRecord(ev_in_done, ds->copy_in)) && ok(cudaStreamWaitEvent(s, ev_in_done, 0)) &&
-                ok(cudaEventRecord(ev_done, ds->copy_out)) && ok(cudaStreamWaitEvent(s, ev_done, 0));
+  cudaEvent_t ev_in_done = ev_alloc;  // reused: the allocation event has been consumed
+  bool joined = ev_in_done && ok(cudaEventRecord(ev_in_done, ds->copy_in)) &&
+                ok(cudaStreamWaitEvent(s, ev_in_done, 0)) && ok(cudaEventRecord(ev_done, ds->copy_out)) &&
+                ok(cudaStreamWaitEvent(s, ev_done, 0));
   if (!joined) {
     // cannot order the release after the copies: wait for them here instead
     cudaStreamSynchronize(ds->copy_in);
@@ -821,8 +835,6 @@ extern "C" FATTN_API int fattn_fwd_host(const void* q, const void* k, const void
     if (rc == FATTN_OK) rc = FATTN_ERR_CUDA;
   }
   if (cudaFreeAsync(buf, s) != cudaSuccess && rc == FATTN_OK) rc = FATTN_ERR_CUDA;
-  for (auto& e : ev)
-    if (e) cudaEventDestroy(e);
   return rc;
 }
 
