@@ -718,16 +718,22 @@ def bwd_arm(args, rank: int, world: int, local_rank: int):
         host_in = [t.cpu().pin_memory() for t in (q, k, v, o, go)] + [lse.cpu().pin_memory()]
         host_out = [torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
         dev_in = [torch.empty_like(t, device=dev) for t in host_in]
-        n_e2e = max(3, min(args.steps, 10))
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
+
+        def e2e_step():
             for hd, dd in zip(host_in, dev_in):
                 dd.copy_(hd, non_blocking=True)
             binding.backward_into(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[5], dev_in[4], dq, dk, dv,
                                   causal=w.causal, scale=w.softmax_scale, key_len=kl)
             for hd, dd in zip(host_out, (dq, dk, dv)):
                 hd.copy_(dd, non_blocking=True)
+
+        for _ in range(2):  # untimed: first copies into these buffers, scratch pool growth
+            e2e_step()
+        n_e2e = max(3, min(args.steps, 10))
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
         torch.cuda.synchronize(dev)
         e2e_s = (time.perf_counter() - t0) / n_e2e
         h2d = sum(t.numel() * t.element_size() for t in host_in)
