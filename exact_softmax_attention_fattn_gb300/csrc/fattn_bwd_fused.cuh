@@ -29,8 +29,8 @@
 // per key tile it sees, in an order that varies from run to run, so dQ is
 // not bit-reproducible) and the zeroing and conversion of the dQ buffer.
 //
-// Measured on the b2h16n4096d128 causal backward: this kernel 338 us against
-// 207 + 158 us for the two-kernel form; the whole call takes 395 us either way.
+// Measured on the b2h16n4096d128 causal backward: this kernel 336 us against
+// 206 + 147 us for the two-kernel form; the whole call 389 us against 378 us.
 // What holds it back is the N = 64 of S^T, dP^T and dQ^T: with both operands
 // in shared memory, a 128 x 64 x 16 MMA reads 6 KB in the 32 tensor cycles it
 // takes, 1.5x the shared-memory bandwidth, so those three GEMMs run at about
