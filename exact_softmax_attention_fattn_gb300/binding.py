@@ -23,8 +23,8 @@ FATTN_ERR_CUDA = 3
 FATTN_ERR_TIMEOUT = 4
 
 EXPORTED = ("fattn_fwd", "fattn_fwd_splitkv", "fattn_fwd_host", "fattn_fwd_noalloc", "fattn_splitkv_plan",
-            "fattn_bwd", "fattn_linear_fwd", "fattn_set_kernel_events", "fattn_status_string", "fattn_last_error",
-            "fattn_version", "fattn_tensor_map_stats")
+            "fattn_unit_schedule", "fattn_bwd", "fattn_linear_fwd", "fattn_set_kernel_events",
+            "fattn_status_string", "fattn_last_error", "fattn_version", "fattn_tensor_map_stats")
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +78,8 @@ def load_library():
             lib.fattn_set_kernel_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
             lib.fattn_splitkv_plan.restype = ctypes.c_int
             lib.fattn_splitkv_plan.argtypes = [ctypes.c_int] * 6
+            lib.fattn_unit_schedule.restype = ctypes.c_longlong
+            lib.fattn_unit_schedule.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_longlong]
             lib.fattn_bwd.restype = ctypes.c_int
             lib.fattn_bwd.argtypes = [ctypes.c_void_p] * 9 + [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
@@ -175,6 +177,20 @@ def splitkv_plan(B: int, H: int, N: int, causal: bool, num_sms: int, n_splits: i
     """fattn_splitkv_plan: key splits per query block the forward uses; host only."""
     return load_library().fattn_splitkv_plan(int(B), int(H), int(N), int(bool(causal)), int(num_sms),
                                              int(n_splits))
+
+
+def unit_schedule(B: int, H: int, N: int, num_ctas: int) -> list[int] | None:
+    """fattn_unit_schedule: the forward's unit per (round, CTA) for a causal call
+    with all keys visible, as a flat list [round * G + cta], or None where the
+    library keeps the snake order; host only."""
+    lib = load_library()
+    n = lib.fattn_unit_schedule(int(B), int(H), int(N), int(num_ctas), None, 0)
+    if n <= 0:
+        return None
+    buf = (ctypes.c_int * n)()
+    if lib.fattn_unit_schedule(int(B), int(H), int(N), int(num_ctas), buf, n) != n:
+        raise FattnError(FATTN_ERR_INVALID_ARG, "fattn_unit_schedule")
+    return list(buf)
 
 
 def bwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, do_ptr: int, lse_ptr: int, dq_ptr: int, dk_ptr: int,

@@ -66,6 +66,15 @@ struct DeviceState {
   // one at a time under host_mu.
   std::mutex host_mu;
   std::vector<cudaEvent_t> host_events;
+  // Unit schedules of recent causal shapes (see round_schedule); a null
+  // table means the snake order is as good.
+  struct Sched {
+    int BH, N, G;
+    std::vector<uint16_t> host;
+    uint16_t* dev;
+  };
+  std::mutex sched_mu;
+  std::vector<Sched> scheds;
 };
 
 std::mutex g_mu;
@@ -622,6 +631,119 @@ extern "C" FATTN_API const char* fattn_status_string(int status) {
 
 namespace {
 
+// ------------------------------------------------------------------------
+// Unit schedule of the persistent forward kernel for causal attention.
+//
+// The kernel deals its units (batch*head, block of 256 query rows), heaviest
+// first, to G CTAs in rounds of G; the snake (CTA c takes unit c of even
+// rounds, G-1-c of odd ones) pairs heavy and light units but leaves the
+// CTAs' totals uneven when the rounds are not whole (on B2 H16 N4096: 512
+// units for 152 CTAs, 123 against a mean of 118 tile steps).  This deals
+// each round's units (the same set as the snake's, so the same K/V working
+// set in each round; the first round, whose CTAs start together, as the
+// snake) so that the totals come out even: the cost of a unit is the tiles
+// its two query tiles visit plus two for its prologue and epilogue, and a
+// deterministic annealing of swaps within a round minimises the squared
+// excess of each CTA's total over the mean.  An empty result: the snake is
+// as good.
+std::vector<uint16_t> build_round_schedule(int BH, int N, int nqb, int G) {
+  const long long units = (long long)BH * nqb;
+  const int R = (int)((units + G - 1) / G);
+  if (R < 2 || G > 65535) return {};
+  auto weight = [&](long long u) -> int {
+    if (u >= units) return 0;
+    const int qb = nqb - 1 - (int)(u / BH);
+    int w = 2;
+    for (int tq = 0; tq < fattn::QT; ++tq) {
+      const int row0 = (qb * fattn::QT + tq) * fattn::BM;
+      if (row0 < N) w += (std::min(N, row0 + fattn::BM) + fattn::BN - 1) / fattn::BN;
+    }
+    return w;
+  };
+  std::vector<uint16_t> pos((size_t)R * G);
+  std::vector<int> w((size_t)R * G), load((size_t)G, 0);
+  long long total = 0;
+  for (int r = 0; r < R; ++r)
+    for (int c = 0; c < G; ++c) {
+      const int slot = (r & 1) ? G - 1 - c : c;
+      pos[(size_t)r * G + c] = (uint16_t)slot;
+      w[(size_t)r * G + slot] = weight((long long)r * G + slot);
+      load[(size_t)c] += w[(size_t)r * G + slot];
+      total += w[(size_t)r * G + slot];
+    }
+  const int snake_max = *std::max_element(load.begin(), load.end());
+  const int target = (int)(total / G);
+  auto excess = [&](int x) { const long long e = std::max(0, x - target); return e * e; };
+  uint64_t rng = 0x9E3779B97F4A7C15ull;
+  auto next = [&]() {
+    rng ^= rng << 13;
+    rng ^= rng >> 7;
+    rng ^= rng << 17;
+    return rng;
+  };
+  std::vector<uint16_t> best = pos;
+  int best_max = snake_max;
+  double temp = 4.0;
+  const int iters = 400000;
+  const double cool = std::pow(0.05 / temp, 1.0 / iters);
+  for (int it = 0; it < iters; ++it, temp *= cool) {
+    const int r = 1 + (int)(next() % (uint64_t)(R - 1));
+    const int c1 = (int)(next() % (uint64_t)G), c2 = (int)(next() % (uint64_t)G);
+    if (c1 == c2) continue;
+    uint16_t& p1 = pos[(size_t)r * G + c1];
+    uint16_t& p2 = pos[(size_t)r * G + c2];
+    const int d = w[(size_t)r * G + p1] - w[(size_t)r * G + p2];
+    if (d == 0) continue;
+    const int n1 = load[(size_t)c1] - d, n2 = load[(size_t)c2] + d;
+    const long long delta = excess(n1) + excess(n2) - excess(load[(size_t)c1]) - excess(load[(size_t)c2]);
+    const double u01 = (double)(next() >> 11) * (1.0 / 9007199254740992.0);
+    if (delta > 0 && u01 >= std::exp(-(double)delta / temp)) continue;
+    std::swap(p1, p2);
+    load[(size_t)c1] = n1;
+    load[(size_t)c2] = n2;
+    if (delta < 0 && std::max(n1, n2) < best_max) {
+      const int m = *std::max_element(load.begin(), load.end());
+      if (m < best_max) {
+        best_max = m;
+        best = pos;
+      }
+    }
+  }
+  if (best_max >= snake_max) return {};
+  return best;
+}
+
+// The device copy of the schedule for (BH, N, G), built and uploaded on
+// first use (not while `s` is being captured into a graph); nullptr: the
+// snake order.
+const uint16_t* round_schedule(DeviceState* ds, int BH, int N, int nqb, int G, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(ds->sched_mu);
+  for (const auto& e : ds->scheds)
+    if (e.BH == BH && e.N == N && e.G == G) return e.dev;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (ds->scheds.size() >= 64) return nullptr;
+  DeviceState::Sched e{BH, N, G, build_round_schedule(BH, N, nqb, G), nullptr};
+  if (!e.host.empty()) {
+    void* dev = nullptr;
+    if (cudaMalloc(&dev, e.host.size() * sizeof(uint16_t)) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (cudaMemcpy(dev, e.host.data(), e.host.size() * sizeof(uint16_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(dev);
+      return nullptr;
+    }
+    e.dev = reinterpret_cast<uint16_t*>(dev);
+  }
+  ds->scheds.push_back(std::move(e));
+  return ds->scheds.back().dev;
+}
+
 // check_pointers = false: the caller owns the buffers (the host-buffer entry
 // point's chunks inside its pool allocation) and has validated the rest.
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -677,6 +799,10 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.wait_limit_ns = wait_limit_ns();
   const int grid = (int)(units < ds->num_sms ? units : ds->num_sms);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // causal, all keys, whole blocks: a schedule that evens out the CTAs' totals
+  p.sched = (p.causal && !key_len && p.n_splits == 1 && d <= 128 && units > grid)
+                ? round_schedule(ds, B * H, N, p.n_qblocks, grid, s)
+                : nullptr;
 
   void* scratch = nullptr;
   if (cudaMallocFromPoolAsync(&scratch, scratch_bytes(B * H, N, d, p.n_kv_tiles, p.n_splits), ds->pool, s) !=
@@ -966,6 +1092,23 @@ extern "C" FATTN_API int fattn_set_kernel_events(void* start, void* stop) {
 extern "C" FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits) {
   if (B <= 0 || H <= 0 || N <= 0 || num_sms <= 0 || n_splits < 0) return 0;
   return plan_splits(B, H, N, causal ? 1 : 0, num_sms, n_splits);
+}
+
+extern "C" FATTN_API long long fattn_unit_schedule(int B, int H, int N, int num_ctas, int* table,
+                                                   long long capacity) {
+  if (B <= 0 || H <= 0 || N <= 0 || num_ctas <= 0) return 0;
+  if ((long long)B * H > 0x7FFFFFFFll) return 0;
+  const int nqb = (N + fattn::QT * fattn::BM - 1) / (fattn::QT * fattn::BM);
+  const long long units = (long long)B * H * nqb;
+  if (units > 0x7FFFFFFFll) return 0;
+  const int G = (int)std::min<long long>(units, num_ctas);
+  const std::vector<uint16_t> pos = build_round_schedule(B * H, N, nqb, G);
+  if (pos.empty()) return 0;
+  const long long n = (long long)pos.size();
+  if (!table) return n;
+  if (capacity < n) return -1;
+  for (long long i = 0; i < n; ++i) table[i] = (int)((i / G) * G + pos[(size_t)i]);
+  return n;
 }
 
 // ------------------------------------------------------------------------
@@ -1293,6 +1436,7 @@ extern "C" FATTN_API int fattn_fwd_noalloc(const void* q, const void* k, const v
   const long long units = (long long)B * H * p.n_qblocks;
   if (units > 0x7FFFFFFFll) return FATTN_ERR_INVALID_ARG;
   p.n_units = (int)units;
+  p.sched = nullptr;  // the snake order: nothing to build or upload during a capture
   p.n_splits = 1;  // no split-KV here: its partials would not fit a fixed array
   p.o_part = nullptr;
   p.head_group = 1;

@@ -95,6 +95,7 @@ struct Params {
   int o_v8;       // O is 32-byte aligned and hd a multiple of 16: rows of O take 32-byte stores
   int n_qblocks;  // ceil(N / 256)
   int n_units;    // B * H * n_qblocks * n_splits
+  const uint16_t* sched;  // nullptr: snake order; else [rounds, G]: CTA c's place in round r's units
   int n_splits;    // K/V splits per query block (1: no split, O and LSE written directly)
   int head_group;  // one-query-tile kernel (head dims above 128): heads per group of its CTA order
   float* o_part;   // n_splits > 1: [n_splits, B*H, N, D] fp32 O / l of each split
@@ -235,7 +236,13 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int kl_raw) 
 // Persistent schedule: CTA c takes, in round r, unit r*G + c (r even) or
 // r*G + G-1-c (r odd).  Units are ordered heaviest first, so the snake pairs
 // heavy and light units on each CTA.
-__device__ __forceinline__ int unit_of(int r, int c, int G) { return r * G + ((r & 1) ? (G - 1 - c) : c); }
+// A host-built table may replace the snake: it deals each round's units
+// (the same set, so the same K/V working set per round) to the CTAs so that
+// their totals come out more even.
+__device__ __forceinline__ int unit_of(const Params& p, int r, int c, int G) {
+  if (p.sched) return r * G + (int)__ldg(p.sched + (r * G + c));
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
 
 // The units of one CTA in schedule order, read one unit ahead: the next
 // unit's key length and first V-tile storage mode are requested once
@@ -252,7 +259,7 @@ struct UnitIter {
   int fetch_at;            // tile index at which the loads are issued (runtime value)
 
   __device__ __forceinline__ static int round_from(const Params& p, int r, int cta, int G) {
-    while (r * G < p.n_units && unit_of(r, cta, G) >= p.n_units) ++r;
+    while (r * G < p.n_units && unit_of(p, r, cta, G) >= p.n_units) ++r;
     return r * G < p.n_units ? r : -1;
   }
   // the two loads for the next unit; cheap enough to sit inside the tile loop
@@ -263,13 +270,13 @@ struct UnitIter {
   }
   __device__ __forceinline__ void locate_next(const Params& p, int cta, int G) {
     r_next = r < 0 ? -1 : round_from(p, r + 1, cta, G);
-    u_next = r_next < 0 ? -1 : unit_of(r_next, cta, G);
+    u_next = r_next < 0 ? -1 : unit_of(p, r_next, cta, G);
     next_bh = u_next < 0 ? 0 : u_next % (p.B * p.H);
     fetch_at = 1;
   }
   __device__ __forceinline__ void begin(const Params& p, int cta, int G) {
     r = round_from(p, 0, cta, G);
-    u = r < 0 ? -1 : unit_of(r, cta, G);
+    u = r < 0 ? -1 : unit_of(p, r, cta, G);
     if (u >= 0) {
       const int bh = u % (p.B * p.H);
       kl_raw = p.key_len ? __ldg(p.key_len + bh / p.H) : p.N;

@@ -231,6 +231,32 @@ FATTN_API int fattn_fwd_host(const void* q, const void* k, const void* v, void* 
 FATTN_API int fattn_splitkv_plan(int B, int H, int N, int causal, int num_sms, int n_splits);
 
 /*
+ * fattn_unit_schedule: the order in which the forward's persistent kernel
+ * deals its work units to CTAs for a causal call with all keys visible
+ * (key_len NULL), no split and head dim up to 128, computed on the host
+ * alone (no GPU, no CUDA call).  A work unit is one batch*head and block of
+ * 256 query rows; units are numbered heaviest first (unit u is block
+ * ceil(N/256) - 1 - u / (B*H) of batch*head u % (B*H)) and taken in rounds of
+ * num_ctas = min(units, SMs).  The kernel's default is the snake (CTA c takes
+ * unit c of even rounds and num_ctas-1-c of odd ones); where some CTAs'
+ * totals then run well above the mean (rounds that do not divide evenly),
+ * the library deals each later round's units (the same set as the snake's)
+ * so that the totals come out even, the first round as the snake.  Work of
+ * a unit: the key tiles its two query tiles visit plus 2.
+ *
+ *   table     host int[capacity] or NULL: on return table[r*num_ctas + c] is
+ *             the unit CTA c takes in round r (units >= B*H*ceil(N/256) are
+ *             empty places of the last round).
+ *   capacity  entries table can hold.
+ *
+ * Returns the number of entries (rounds * num_ctas) of the table when the
+ * library uses one for this shape (written to table unless table is NULL),
+ * 0 when it keeps the snake (or for B, H, N or num_ctas <= 0), -1 when table
+ * is not NULL and capacity is below that number (nothing written).
+ */
+FATTN_API long long fattn_unit_schedule(int B, int H, int N, int num_ctas, int* table, long long capacity);
+
+/*
  * fattn_linear_fwd: causal linear attention, the second workload ("Linear
  * Attention CUDA kernel" page: CausalLinearAttention.forward with its causal
  * dot product and normaliser):
